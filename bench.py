@@ -1,0 +1,453 @@
+"""Benchmark: aggregated gradient GB/s on one GB300 and its fraction of the
+HBM roofline, with the CPU oracle as the baseline.
+
+One step is one pass of the whole hot path over one batch of synthetic input:
+  1. dense ring all-reduce with the 1/N average, C2 workload: N = 8 ranks x
+     M = 25,557,032 fp32 (a ResNet-50-sized flat gradient), in place;
+  2. Random SkipReduce with skip fraction 0.5 (k = 4 of the 8 Reduce-Scatter
+     steps, seed 0, iteration count = the step number) on the same buffers;
+  3. sparse COO aggregation of the C4 embedding gradient (8 ranks x 335,544
+     entries over a dense size of 33,554,432, 60 % of entries in the first
+     1/8 of the range) into 8 h0 partitions;
+  4. the push-side h0 partition of rank 0's C4 list.
+Algorithmic ("roofline") bytes per step: dense (N-k)*M*4 read + N*M*4 written
+per call; sparse sum(nnz)*8 read + U*8 written + offsets; partition nnz*8 read
+and written.  GB/s = those bytes / device time; the roofline fraction divides
+by the measured HBM copy bandwidth.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+With N > 1 (torchrun) every rank runs an independent replica of the whole
+workload on its own GPU (the path has no exchange between GPUs: replicas
+only); value = bytes of all ranks / the slowest rank's time.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "aggregated gradient GB/s at 1 GB300 and % of HBM roofline, vs host-oracle"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = ("C2 dense ring all-reduce N=8 M=25,557,032 fp32 (plain + Random SkipReduce p=0.5) "
+            "+ C4 sparse COO union into 8 h0 partitions (N=8, M=33,554,432, 1% density) "
+            "+ push-side partition of one C4 list")
+
+# DRAM traffic of the dominant kernel from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum per launch), valid only while the kernel source is the
+# one that was profiled.  The command that produced it is in profiles/.
+TRAFFIC = {
+    "ring_fused_kernel<float>": {"source_sha256": None, "bytes_per_launch": None},
+}
+
+# Kernel launches each library call makes (counted from the library source).
+LAUNCHES = {"ring": 1, "skip": 1, "sparse": 4, "partition": 3}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        return summarize_clocks(self.lines)
+
+
+def summarize_clocks(lines):
+    sm, mx, reasons = [], [], set()
+    names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    for ln in lines:
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            mx.append(float(parts[2]))
+        except ValueError:
+            continue
+        for name, v in zip(names, parts[5:9]):
+            if v.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workload
+class Workload:
+    """Device-resident inputs and outputs of one step."""
+
+    def __init__(self, torch, zr, dev):
+        import numpy as np
+
+        import workloads
+
+        self.torch, self.zr, self.dev = torch, zr, dev
+        c2 = workloads.DENSE_C2
+        self.n, self.m, self.k = c2["n"], c2["m"], c2["skip_k"]
+        self.seed = c2["skip_seed"]
+        self.host_dense = workloads.dense_c2()
+        self.dense = torch.from_numpy(self.host_dense).to(dev)
+        self.bufs = [self.dense[r] for r in range(self.n)]
+        c4 = workloads.SPARSE_C4
+        self.m4, self.parts = c4["m"], c4["n_parts"]
+        self.part_seed = c4["part_seed"]
+        idx_l, val_l = workloads.sparse_c4()
+        self.host_idx = [np.ascontiguousarray(a) for a in idx_l]
+        self.host_val = [np.ascontiguousarray(v) for v in val_l]
+        self.d_idx = [torch.from_numpy(a).to(dev) for a in self.host_idx]
+        self.d_val = [torch.from_numpy(v).to(dev) for v in self.host_val]
+        self.nnz = [int(a.size) for a in self.host_idx]
+        self.work = zr.SparseWorkspace(self.n, self.m4, self.parts, sum(self.nnz), dev)
+        self.p_out_idx = torch.empty(self.nnz[0], dtype=torch.int32, device=dev)
+        self.p_out_val = torch.empty(self.nnz[0], dtype=torch.float32, device=dev)
+        self.p_off = torch.empty(self.parts + 1, dtype=torch.int64, device=dev)
+        self.p_ws = torch.empty(zr.zr_partition_workspace_size(self.nnz[0], self.parts),
+                                dtype=torch.uint8, device=dev)
+        # Union size of C4 (fixed by the inputs): run once and read it.
+        zr.sparse_aggregate(self.d_idx, self.d_val, self.m4, self.parts, self.part_seed,
+                            work=self.work)
+        torch.cuda.synchronize()
+        self.union = int(self.work.out_nnz.item())
+
+    def bytes(self):
+        s = 4
+        dense_plain = 2 * self.n * self.m * s
+        dense_skip = (self.n - self.k) * self.m * s + self.n * self.m * s
+        sparse = sum(self.nnz) * 8 + self.union * 8 + (self.parts + 1) * 8 + 8
+        part = self.nnz[0] * 8 * 2 + (self.parts + 1) * 8
+        return {"dense_plain": dense_plain, "dense_skip": dense_skip, "sparse": sparse,
+                "partition": part}
+
+    def step(self, i, events=None):
+        zr = self.zr
+        ev = events or {}
+        if "ring" in ev:
+            ev["ring"][0].record()
+        zr.ring_allreduce(self.bufs, average=True)
+        if "ring" in ev:
+            ev["ring"][1].record()
+        zr.skipreduce(self.bufs, k=self.k, mode=zr.ZR_SKIP_RANDOM, seed=self.seed, step=i)
+        if "skip" in ev:
+            ev["skip"][1].record()
+        zr.sparse_aggregate(self.d_idx, self.d_val, self.m4, self.parts, self.part_seed,
+                            work=self.work)
+        if "sparse" in ev:
+            ev["sparse"][1].record()
+        zr.partition(self.d_idx[0], self.d_val[0], self.parts, self.part_seed, self.p_out_idx,
+                     self.p_out_val, self.p_off, self.p_ws)
+        if "partition" in ev:
+            ev["partition"][1].record()
+
+
+def timed_device(torch, W, steps, warmup):
+    for i in range(warmup):
+        W.step(i)
+    torch.cuda.synchronize()
+    names = ("ring", "skip", "sparse", "partition")
+    per = {n: [] for n in names}
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    evs = []
+    for i in range(steps):
+        e = {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for n in names}
+        # each component starts where the previous one ended
+        e["skip"] = (e["ring"][1], e["skip"][1])
+        e["sparse"] = (e["skip"][1], e["sparse"][1])
+        e["partition"] = (e["sparse"][1], e["partition"][1])
+        evs.append(e)
+    start.record()
+    for i in range(steps):
+        W.step(warmup + i, evs[i])
+    stop.record()
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(stop)
+    for e in evs:
+        for n in names:
+            per[n].append(e[n][0].elapsed_time(e[n][1]))
+    return total_ms, per
+
+
+def timed_e2e(torch, W, steps):
+    """Same step through the public API from pinned host buffers: every step
+    copies its inputs host->device and reads the results back."""
+    import numpy as np
+
+    zr = W.zr
+    h_dense = torch.from_numpy(W.host_dense).pin_memory()
+    h_idx = [torch.from_numpy(a).pin_memory() for a in W.host_idx]
+    h_val = [torch.from_numpy(v).pin_memory() for v in W.host_val]
+    out_dense = torch.empty(W.m, dtype=torch.float32).pin_memory()
+    cap = sum(W.nnz)
+    out_idx = torch.empty(cap, dtype=torch.int32).pin_memory()
+    out_val = torch.empty(cap, dtype=torch.float32).pin_memory()
+    out_off = torch.empty(W.parts + 1, dtype=torch.int64).pin_memory()
+    p_idx = torch.empty(W.nnz[0], dtype=torch.int32).pin_memory()
+    p_val = torch.empty(W.nnz[0], dtype=torch.float32).pin_memory()
+    h2d = h_dense.numel() * 4 + sum(a.numel() * 8 for a in h_idx)
+    d2h = W.m * 4 + W.union * 8 + (W.parts + 1) * 8 + W.nnz[0] * 8
+
+    def one(i):
+        W.dense.copy_(h_dense, non_blocking=True)
+        for r in range(W.n):
+            W.d_idx[r].copy_(h_idx[r], non_blocking=True)
+            W.d_val[r].copy_(h_val[r], non_blocking=True)
+        W.step(i)
+        out_dense.copy_(W.dense[0], non_blocking=True)
+        out_idx[:W.union].copy_(W.work.out_idx[:W.union], non_blocking=True)
+        out_val[:W.union].copy_(W.work.out_val[:W.union], non_blocking=True)
+        out_off.copy_(W.work.offsets[:W.parts + 1], non_blocking=True)
+        p_idx.copy_(W.p_out_idx, non_blocking=True)
+        p_val.copy_(W.p_out_val, non_blocking=True)
+
+    one(0)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(steps):
+        one(i + 1)
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    assert np.isfinite(float(out_dense[0]))
+    return ms, h2d, d2h
+
+
+# ---------------------------------------------------------------- oracle
+def oracle_sample(budget_s=12.0):
+    """Time the CPU oracle, as it stands, on a bounded sample of the step's
+    workload: the dense plain ring and the SkipReduce call on the first
+    M' elements of every C2 rank (M' a multiple of N), and the full C4 sparse
+    aggregation plus the partition of rank 0's list.  Returns a dict with
+    the GB/s over the sample's algorithmic bytes."""
+    import numpy as np
+
+    import workloads
+    from oracle import ring as oring
+    from oracle import sparse as osparse
+
+    c2 = workloads.DENSE_C2
+    n, k = c2["n"], c2["skip_k"]
+    mp = (1 << 21)
+    x = workloads.dense_f32_per_rank(n, mp, c2["sigma"], 200)
+    c4 = workloads.SPARSE_C4
+    idx_l, val_l = workloads.sparse_c4()
+    nbytes = 0
+    t_total = 0.0
+    reps = 0
+    t_start = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        y = oring.allreduce_f32(x, divisor=oring.DIV_N)
+        o = oring.skip_offset(oring.SKIP_RANDOM, k, c2["skip_seed"], reps, n)
+        oring.allreduce_f32(y, k=k, o=o, divisor=oring.DIV_N)
+        ui, uv, off = osparse.aggregate(idx_l, val_l, c4["n_parts"], c4["part_seed"])
+        osparse.partition(idx_l[0], val_l[0], c4["n_parts"], c4["part_seed"])
+        t_total += time.perf_counter() - t0
+        reps += 1
+        nbytes += (2 * n * mp * 4 + (2 * n - k) * mp * 4 + sum(a.size for a in idx_l) * 8
+                   + ui.size * 8 + (c4["n_parts"] + 1) * 8 + 8 + idx_l[0].size * 16
+                   + (c4["n_parts"] + 1) * 8)
+        if time.perf_counter() - t_start > budget_s:
+            break
+    return {
+        "value": nbytes / t_total / 1e9,
+        "unit": UNIT,
+        "cores": 1,
+        "kind": "oracle",
+        "sample": ("%d repetitions of: literal ring + Random SkipReduce (k=4) on 8 ranks x %d fp32 "
+                   "(the first %d elements of each C2 rank), full C4 sparse union + 8-way partition "
+                   "and rank-0 push partition; numpy, single-threaded" % (reps, mp, mp)),
+        "seconds": t_total,
+        "host_threads_available": len(os.sched_getaffinity(0)),
+    }
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    res = oracle_sample(budget_s=max(5.0, min(60.0, 4.0 * args.steps)))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": res["value"], "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": res["sample"]},
+        "cpu_baseline": res,
+        "e2e": {"value": res["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- main
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+
+    import __graft_entry__
+
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    __graft_entry__.build()
+    import gradient_synchronisation_gb300 as zr
+
+    W = Workload(torch, zr, dev)
+    b = W.bytes()
+    step_bytes = sum(b.values())
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    total_ms, per = timed_device(torch, W, args.steps, args.warmup)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+    torch.cuda.synchronize()
+
+    value = world * step_bytes * args.steps / (total_ms / 1e3) / 1e9
+    peak, peak_kind = measured_hbm()
+    ring_ms = statistics.mean(per["ring"] + per["skip"])
+    ring_bytes = (b["dense_plain"] + b["dense_skip"]) / 2
+    achieved = ring_bytes / (ring_ms / 1e3) / 1e9
+    tr = TRAFFIC["ring_fused_kernel<float>"]
+    sha = source_sha(os.path.join(ROOT, "gradient_synchronisation_gb300", "csrc", "ring.cu"))
+    traffic = tr["bytes_per_launch"] if tr["source_sha256"] == sha else None
+
+    parts = {}
+    for name, key in (("ring", "dense_plain"), ("skip", "dense_skip"), ("sparse", "sparse"),
+                      ("partition", "partition")):
+        ms = statistics.median(per[name])
+        parts[name] = {"bytes": b[key], "median_ms": ms, "gbs": b[key] / (ms / 1e3) / 1e9,
+                       "frac": b[key] / (ms / 1e3) / 1e9 / peak}
+
+    e2e = None
+    if not args.no_e2e:
+        e_ms, h2d, d2h = timed_e2e(torch, W, max(2, min(args.steps, 5)))
+        steps_e = max(2, min(args.steps, 5))
+        e2e = {"value": world * step_bytes * steps_e / (e_ms / 1e3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "bytes_per_step": step_bytes,
+                       "l2": "inputs larger than L2 (dense ranks 818 MB resident; the dense "
+                             "traffic evicts the sparse inputs between steps)",
+                       "parallelism": "replicas only" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "ring_fused_kernel<float> (C2 plain + SkipReduce launches)",
+                         "peak_source": peak_kind},
+            "parts": parts,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clk,
+            "gpu_launches": sum(LAUNCHES.values()) * args.steps,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

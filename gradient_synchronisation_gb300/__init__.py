@@ -1,0 +1,274 @@
+"""gradient_synchronisation_gb300 -- Python binding of libzr (``include/zr.h``).
+
+Gradient aggregation across N data-parallel ranks whose buffers all live in
+one GPU's memory: the ring all-reduce with SkipReduce slice skipping and the
+fused average (dense), and the Zen-style COO union with rank-ordered sums and
+the h0 partition (sparse).  Every step runs in the library's CUDA kernels;
+this module only marshals arguments (pointers, sizes, the stream handle) into
+the C ABI.  There is no CPU fallback: the library is loaded on the first call,
+and if ``libzr.so`` has not been built that call raises ImportError.  (Loading
+lazily lets ``gradient_synchronisation_gb300._build`` run before the library
+exists.)
+
+Two layers:
+
+* ``zr_ring_allreduce``, ``zr_skipreduce``, ``zr_sparse_aggregate``,
+  ``zr_partition``, ``zr_query_status`` ... -- the C entry points under their
+  own names, taking integers for pointers and streams; they return the
+  ``zr_status`` code.
+* ``ring_allreduce``, ``skipreduce``, ``sparse_aggregate``, ``partition`` --
+  the same calls taking torch CUDA tensors, raising ``ZrError`` on a non-OK
+  status.  PyTorch supplies device memory and the current stream only.
+"""
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libzr.so")
+
+ZR_OK = 0
+ZR_ERR_INVALID_ARG = 1
+ZR_ERR_UNSUPPORTED = 2
+ZR_ERR_ALIGNMENT = 3
+ZR_ERR_CAPACITY = 4
+ZR_ERR_INPUT_UNSORTED = 5
+ZR_ERR_TIMEOUT = 6
+ZR_ERR_CUDA = 7
+
+ZR_F32 = 0
+ZR_BF16 = 1
+ZR_SKIP_STATIC = 0
+ZR_SKIP_RANDOM = 1
+ZR_DIV_N = 0
+ZR_DIV_N_MINUS_K = 1
+ZR_DIV_NONE = 2
+ZR_MAX_RANKS = 64
+ZR_MAX_PARTS = 256
+
+EXPORTS = (
+    "zr_ring_allreduce", "zr_skipreduce", "zr_sparse_aggregate", "zr_sparse_workspace_size",
+    "zr_partition", "zr_partition_workspace_size", "zr_query_status", "zr_status_string",
+    "zr_version",
+)
+
+
+class ZrError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, status_string(status), status))
+
+
+class SkipCfg(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("k", ctypes.c_int32), ("seed", ctypes.c_uint64),
+                ("step", ctypes.c_uint64), ("divisor", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libzr.so is not built (%s); run gradient_synchronisation_gb300._build.build()"
+                          % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.c_void_p
+    i32, i64, u64, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
+    PP = ctypes.POINTER(ctypes.c_void_p)
+    sig = {
+        "zr_ring_allreduce": (i32, [PP, i32, i64, i32, i32, P]),
+        "zr_skipreduce": (i32, [PP, i32, i64, i32, ctypes.POINTER(SkipCfg), P]),
+        "zr_sparse_aggregate": (i32, [PP, PP, ctypes.POINTER(i64), i32, i64, i32, u64, i32, P, P,
+                                      i64, P, P, P, sz, P]),
+        "zr_sparse_workspace_size": (sz, [i32, i64, i32]),
+        "zr_partition": (i32, [P, P, i64, i32, u64, P, P, P, P, sz, P]),
+        "zr_partition_workspace_size": (sz, [i64, i32]),
+        "zr_query_status": (i32, [P, P, ctypes.POINTER(i32)]),
+        "zr_status_string": (ctypes.c_char_p, [i32]),
+        "zr_version": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib_handle = None
+
+
+def lib():
+    """The loaded libzr (ctypes.CDLL); loads it on first use."""
+    global _lib_handle
+    if _lib_handle is None:
+        _lib_handle = _load()
+    return _lib_handle
+
+
+def _ptrs(values):
+    arr = (ctypes.c_void_p * max(1, len(values)))()
+    for i, v in enumerate(values):
+        arr[i] = v
+    return arr
+
+
+# ------------------------------------------------------------ C entry points
+def zr_ring_allreduce(bufs, n, m, dtype, average, stream):
+    return lib().zr_ring_allreduce(_ptrs(bufs), n, m, dtype, average, stream)
+
+
+def zr_skipreduce(bufs, n, m, dtype, cfg, stream):
+    return lib().zr_skipreduce(_ptrs(bufs), n, m, dtype, ctypes.byref(cfg), stream)
+
+
+def zr_sparse_aggregate(idx, val, nnz, n, dense_size, n_parts, part_seed, average, out_idx,
+                        out_val, out_cap, d_out_nnz, d_offsets, ws, ws_bytes, stream):
+    nnz_arr = (ctypes.c_int64 * max(1, len(nnz)))(*nnz)
+    return lib().zr_sparse_aggregate(_ptrs(idx), _ptrs(val), nnz_arr, n, dense_size, n_parts,
+                                    part_seed, average, out_idx, out_val, out_cap, d_out_nnz,
+                                    d_offsets, ws, ws_bytes, stream)
+
+
+def zr_sparse_workspace_size(n, dense_size, n_parts):
+    return lib().zr_sparse_workspace_size(n, dense_size, n_parts)
+
+
+def zr_partition(idx, val, nnz, n_parts, part_seed, out_idx, out_val, d_offsets, ws, ws_bytes,
+                 stream):
+    return lib().zr_partition(idx, val, nnz, n_parts, part_seed, out_idx, out_val, d_offsets, ws,
+                             ws_bytes, stream)
+
+
+def zr_partition_workspace_size(nnz, n_parts):
+    return lib().zr_partition_workspace_size(nnz, n_parts)
+
+
+def zr_query_status(ws, stream):
+    out = ctypes.c_int32(-1)
+    st = lib().zr_query_status(ws, stream, ctypes.byref(out))
+    if st != ZR_OK:
+        raise ZrError(st, "zr_query_status")
+    return out.value
+
+
+def status_string(status):
+    return lib().zr_status_string(status).decode()
+
+
+def version():
+    return lib().zr_version().decode()
+
+
+# ------------------------------------------------------------ torch wrappers
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _dtype_code(t):
+    import torch
+
+    if t.dtype == torch.float32:
+        return ZR_F32
+    if t.dtype == torch.bfloat16:
+        return ZR_BF16
+    raise TypeError("dense buffers must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _check(st, where):
+    if st != ZR_OK:
+        raise ZrError(st, where)
+
+
+def _dense_args(bufs):
+    if len(bufs) == 0:
+        raise ValueError("need at least one rank buffer")
+    m = bufs[0].numel()
+    dt = _dtype_code(bufs[0])
+    for b in bufs:
+        if not b.is_cuda or not b.is_contiguous() or b.numel() != m or _dtype_code(b) != dt:
+            raise ValueError("rank buffers must be contiguous CUDA tensors of one size and dtype")
+    return [b.data_ptr() for b in bufs], len(bufs), m, dt
+
+
+def ring_allreduce(bufs, average=True, stream=None):
+    """In-place ring all-reduce of the rank buffers ``bufs`` (list of tensors)."""
+    ptrs, n, m, dt = _dense_args(bufs)
+    _check(zr_ring_allreduce(ptrs, n, m, dt, 1 if average else 0, _stream(stream)),
+           "zr_ring_allreduce")
+
+
+def skipreduce(bufs, k, mode=ZR_SKIP_RANDOM, seed=0, step=0, divisor=ZR_DIV_N, stream=None):
+    """In-place SkipReduce all-reduce skipping ``k`` Reduce-Scatter steps."""
+    ptrs, n, m, dt = _dense_args(bufs)
+    cfg = SkipCfg(mode, k, seed, step, divisor, 0)
+    _check(zr_skipreduce(ptrs, n, m, dt, cfg, _stream(stream)), "zr_skipreduce")
+
+
+def skip_fraction_to_k(p, n):
+    """SkipReduce skip fraction p -> number of skipped steps k = p*N (the pages:
+    skipping k Reduce-Scatter steps skips k/N of the gradients)."""
+    k = p * n
+    if abs(k - round(k)) > 1e-9 or not (0 <= round(k) <= n - 1):
+        raise ValueError("skip fraction %r needs p*N to be an integer in [0, N-1]" % (p,))
+    return int(round(k))
+
+
+class SparseWorkspace:
+    """Device workspace and outputs for ``sparse_aggregate`` (torch-allocated)."""
+
+    def __init__(self, n, dense_size, n_parts, capacity, device):
+        import torch
+
+        ws_bytes = zr_sparse_workspace_size(n, dense_size, n_parts)
+        if ws_bytes == 0:
+            raise ValueError("invalid sparse workspace request")
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+        self.out_idx = torch.empty(max(1, capacity), dtype=torch.int32, device=device)
+        self.out_val = torch.empty(max(1, capacity), dtype=torch.float32, device=device)
+        self.out_nnz = torch.zeros(1, dtype=torch.int64, device=device)
+        self.offsets = torch.zeros(max(n_parts, 1) + 1, dtype=torch.int64, device=device)
+        self.capacity = capacity
+        self.n_parts = n_parts
+
+
+def sparse_aggregate(idx_list, val_list, dense_size, n_parts, part_seed=0, average=False,
+                     work=None, stream=None):
+    """Union with rank-ordered sums, partitioned by h0.  Returns the workspace
+    object whose ``out_idx``/``out_val``/``out_nnz``/``offsets`` hold the result
+    (device tensors; nothing is copied to the host)."""
+    n = len(idx_list)
+    nnz = [int(a.numel()) for a in idx_list]
+    for a, v in zip(idx_list, val_list):
+        if a.dtype.itemsize != 4 or not a.is_cuda or not v.is_cuda or a.numel() != v.numel():
+            raise ValueError("idx must be int32 and val float32 CUDA tensors of equal length")
+    if work is None:
+        work = SparseWorkspace(n, dense_size, n_parts, sum(nnz), idx_list[0].device)
+    st = zr_sparse_aggregate([a.data_ptr() for a in idx_list], [v.data_ptr() for v in val_list],
+                             nnz, n, dense_size, n_parts, part_seed, 1 if average else 0,
+                             work.out_idx.data_ptr(), work.out_val.data_ptr(), work.capacity,
+                             work.out_nnz.data_ptr(), work.offsets.data_ptr(), work.ws.data_ptr(),
+                             work.ws.numel(), _stream(stream))
+    _check(st, "zr_sparse_aggregate")
+    return work
+
+
+def partition(idx, val, n_parts, part_seed=0, out_idx=None, out_val=None, offsets=None, ws=None,
+              stream=None):
+    """Stable h0 partition of one COO list; returns (out_idx, out_val, offsets)."""
+    import torch
+
+    nnz = int(idx.numel())
+    dev = idx.device
+    out_idx = torch.empty(max(1, nnz), dtype=torch.int32, device=dev) if out_idx is None else out_idx
+    out_val = torch.empty(max(1, nnz), dtype=torch.float32, device=dev) if out_val is None else out_val
+    offsets = torch.empty(n_parts + 1, dtype=torch.int64, device=dev) if offsets is None else offsets
+    if ws is None:
+        ws = torch.empty(max(16, zr_partition_workspace_size(nnz, n_parts)), dtype=torch.uint8,
+                         device=dev)
+    st = zr_partition(idx.data_ptr(), val.data_ptr(), nnz, n_parts, part_seed, out_idx.data_ptr(),
+                      out_val.data_ptr(), offsets.data_ptr(), ws.data_ptr(), ws.numel(),
+                      _stream(stream))
+    _check(st, "zr_partition")
+    return out_idx, out_val, offsets

@@ -1,0 +1,215 @@
+/*
+ * zr.h -- C ABI of libzr: gradient aggregation across N data-parallel ranks
+ * whose buffers all live in one GPU's memory.
+ *
+ * Pages the operations follow (cited by title and section):
+ *   [SR]  "SkipReduce: (Interconnection) Network Sparsity to Accelerate
+ *         Distributed Machine Learning" (MICRO'25 digest)
+ *   [ZEN] "Zen: Empowering Distributed Training with Sparsity-driven Data
+ *         Synchronization" (OSDI'25 digest)
+ *   [CMU] "15642 Machine Learning Systems: Distributed Training and
+ *         Parallelization" (CMU course notes)
+ *
+ * Conventions for every entry point:
+ *   - Pointers named d_* / device buffers are CUDA device pointers; arrays of
+ *     pointers (bufs, idx, val) and count arrays (nnz) are HOST arrays.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call is stream-ordered and asynchronous: it validates
+ *     its arguments on the host, enqueues its kernels and returns.  Nothing
+ *     is copied back to the host and nothing synchronises.
+ *   - The caller owns every buffer, including the workspace `ws`; the library
+ *     allocates no device or host memory.
+ *   - The return value reports argument errors (checked before anything is
+ *     enqueued; on error nothing is enqueued and no buffer is touched) and
+ *     launch errors (ZR_ERR_CUDA).  Errors found by a kernel on the device
+ *     (an unsorted or out-of-range sparse index) are written to a status
+ *     word inside `ws`; read it with zr_query_status after the stream work.
+ *   - No C++ exception crosses this interface.
+ */
+#ifndef ZR_H
+#define ZR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum zr_status {
+  ZR_OK = 0,
+  ZR_ERR_INVALID_ARG = 1,    /* a size, count, pointer or flag is out of range */
+  ZR_ERR_UNSUPPORTED = 2,    /* a valid request this build does not implement */
+  ZR_ERR_ALIGNMENT = 3,      /* a dense rank buffer or a workspace is not
+                                16-byte aligned */
+  ZR_ERR_CAPACITY = 4,       /* an output or workspace buffer is too small */
+  ZR_ERR_INPUT_UNSORTED = 5, /* device-detected: sparse indices not strictly
+                                ascending or outside [0, dense_size) */
+  ZR_ERR_TIMEOUT = 6,        /* device-detected: a bounded wait gave up */
+  ZR_ERR_CUDA = 7            /* a CUDA runtime call or launch failed */
+} zr_status;
+
+typedef enum zr_dtype {
+  ZR_F32 = 0,  /* IEEE binary32 */
+  ZR_BF16 = 1  /* bfloat16: widened exactly to fp32, accumulated in fp32,
+                  rounded once (round-to-nearest-even) on output */
+} zr_dtype;
+
+#define ZR_MAX_RANKS 64
+#define ZR_MAX_PARTS 256
+
+/* SkipReduce slice choice [SR section 4.2 (Static), section 4.3 (Random)]. */
+typedef enum zr_skip_mode {
+  ZR_SKIP_STATIC = 0, /* offset o = 0: slice c omits ranks c .. c+k-1 */
+  ZR_SKIP_RANDOM = 1  /* offset o drawn from (seed, step), see zr_skip_cfg */
+} zr_skip_mode;
+
+/* What the reduced slice is divided by [SR section 4.1, and section 5's
+ * SkipReduce vs DropReduce comparison]. */
+typedef enum zr_divisor {
+  ZR_DIV_N = 0,         /* SkipReduce average: skipped slices count as zero */
+  ZR_DIV_N_MINUS_K = 1, /* DropReduce: skipped slices are removed */
+  ZR_DIV_NONE = 2       /* plain sum */
+} zr_divisor;
+
+/*
+ * SkipReduce configuration.
+ *   mode     ZR_SKIP_STATIC or ZR_SKIP_RANDOM.
+ *   k        Reduce-Scatter steps skipped, 0 <= k <= n-1 [SR Algorithm 2:
+ *            the loop runs s = k .. N-2].  A skip fraction p maps to k = p*N.
+ *   seed     Random mode: generator seed shared by every rank.
+ *   step     Random mode: the iteration count [SR section 4.3].
+ *   divisor  a zr_divisor value.
+ * Random offset: o = floor(hi32(x) * n / 2^32), where x is output number
+ * `step` (0-based) of SplitMix64 seeded with `seed` (Steele, Lea and Flood,
+ * OOPSLA 2014): x = mix(seed + (step + 1) * 0x9E3779B97F4A7C15 mod 2^64),
+ * mix(z) = z ^= z>>30; z *= 0xBF58476D1CE4E5B9; z ^= z>>27;
+ *          z *= 0x94D049BB133111EB; z ^= z>>31.
+ * With k = 0 the offset is 0 in both modes (p = 0 is exactly the plain ring).
+ */
+typedef struct zr_skip_cfg {
+  int32_t mode;
+  int32_t k;
+  uint64_t seed;
+  uint64_t step;
+  int32_t divisor;
+  int32_t reserved; /* must be 0 */
+} zr_skip_cfg;
+
+/*
+ * Ring all-reduce, in place [CMU "Ring AllReduce"; SR section 2 and
+ * Algorithm 1 with p = 0].
+ *
+ * bufs     host array of n device pointers; bufs[r] is rank r's buffer of m
+ *          elements of type dt, 16-byte aligned, pairwise non-overlapping.
+ * n        ranks, 1 <= n <= ZR_MAX_RANKS.   m: elements per rank, >= 0.
+ * average  0: every rank ends with the sum; 1: with the sum / n.
+ *
+ * Result, bit for bit: the tensor is cut into n slices of C = ceil(m/n)
+ * elements (the last ones may be short or empty).  Element e of slice c ends,
+ * on every rank, as fl(...fl(fl(g_c[e] + g_{c+1}[e]) + g_{c+2}[e]) ... +
+ * g_{c+n-1}[e]) (ranks mod n; each + one fp32 RNE addition) -- the order in
+ * which the Reduce-Scatter accumulates slice c, starting at the rank that
+ * first sends it -- then divided by n with one fp32 RNE division when
+ * average = 1, then (bf16) rounded once to bf16.  AllGather copies it to all
+ * ranks.  m = 0 or n = 1 with average = 0 changes nothing.
+ */
+zr_status zr_ring_allreduce(void* const* bufs, int32_t n, int64_t m, zr_dtype dt,
+                            int32_t average, void* stream);
+
+/*
+ * SkipReduce all-reduce, in place [SR section 4.2 Algorithm 2, section 4.3].
+ *
+ * Arguments as zr_ring_allreduce, plus cfg (host pointer, see zr_skip_cfg).
+ * Result: slice c is folded as above but starting at rank
+ * s_c = (c + k - o) mod n and over the n - k ranks s_c .. s_c+n-k-1 only;
+ * the k skipped ranks' values are not read.  The divisor is n, n - k or none.
+ * With k = 0 and divisor ZR_DIV_N the result equals
+ * zr_ring_allreduce(average = 1) bit for bit.
+ */
+zr_status zr_skipreduce(void* const* bufs, int32_t n, int64_t m, zr_dtype dt,
+                        const zr_skip_cfg* cfg, void* stream);
+
+/*
+ * Sparse (COO) aggregation with partitioning [ZEN section 2.1 (COO), Problem
+ * 1, section 3.2 Technique #3 and Algorithm 1's first-level hash h0].
+ *
+ * idx, val, nnz  host arrays of n entries: rank r's list is nnz[r] entries at
+ *                device pointers idx[r] (int32, strictly ascending, each in
+ *                [0, dense_size)) and val[r] (fp32).  nnz[r] may be 0 (its
+ *                pointers are then ignored).
+ * n              ranks, 1 <= n <= ZR_MAX_RANKS.
+ * dense_size     M, the dense tensor size, 1 <= M <= 2^31 - 1.
+ * n_parts        partitions (servers), 0 <= n_parts <= ZR_MAX_PARTS;
+ *                0 = no partitioning (plain ascending union).
+ * part_seed      seed of h0.
+ * average        0: sums; 1: sums divided once by n (fp32 RNE).
+ * out_idx, out_val  device outputs of out_cap entries; out_cap must be at
+ *                least sum(nnz) (checked here, so the kernels cannot write
+ *                past it).
+ * d_out_nnz      device int64: receives U, the union size.
+ * d_offsets      device int64[n_parts + 1]: partition j is
+ *                [d_offsets[j], d_offsets[j+1]); may be NULL if n_parts = 0.
+ * ws, ws_bytes   device workspace of at least
+ *                zr_sparse_workspace_size(n, dense_size, n_parts) bytes,
+ *                16-byte aligned.  Its first 4 bytes are the status word.
+ *
+ * Result: one entry per index in the union of the n lists.  Its value is the
+ * left fold, in ascending rank order, of the values of the ranks that hold
+ * the index, starting from the first holder's value (fp32 RNE additions).
+ * Partition of index x: h(x) = ((a*x + b) mod 2^64) >> 32,
+ * p(x) = (h(x) * n_parts) >> 32, with a = (SplitMix64(part_seed) output 0) | 1
+ * and b = output 1.  Entries are written partition-major, ascending index
+ * inside each partition.
+ * If an input list is not strictly ascending or holds an index outside
+ * [0, dense_size), the status word becomes ZR_ERR_INPUT_UNSORTED and the
+ * outputs are unspecified (every access still stays inside the buffers).
+ */
+zr_status zr_sparse_aggregate(const int32_t* const* idx, const float* const* val,
+                              const int64_t* nnz, int32_t n, int64_t dense_size,
+                              int32_t n_parts, uint64_t part_seed, int32_t average,
+                              int32_t* out_idx, float* out_val, int64_t out_cap,
+                              int64_t* d_out_nnz, int64_t* d_offsets,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes zr_sparse_aggregate needs (0 on invalid arguments). */
+size_t zr_sparse_workspace_size(int32_t n, int64_t dense_size, int32_t n_parts);
+
+/*
+ * Push-side partition of one rank's COO list [ZEN Problem 1, requirement 1:
+ * each worker splits its nonzeros into n parts with the shared h0].
+ *
+ * idx, val   device inputs of nnz entries (any order; indices need not be
+ *            unique).  out_idx, out_val: device outputs of nnz entries.
+ * d_offsets  device int64[n_parts + 1].   1 <= n_parts <= ZR_MAX_PARTS.
+ * ws         device workspace of zr_partition_workspace_size(nnz, n_parts)
+ *            bytes, 16-byte aligned.
+ * Result: entries grouped by p(idx) (same h0 as above), partition-major; inside
+ * a partition entries keep their input order (a stable split).
+ */
+zr_status zr_partition(const int32_t* idx, const float* val, int64_t nnz,
+                       int32_t n_parts, uint64_t part_seed, int32_t* out_idx,
+                       float* out_val, int64_t* d_offsets, void* ws,
+                       size_t ws_bytes, void* stream);
+
+/* Workspace bytes zr_partition needs (0 on invalid arguments). */
+size_t zr_partition_workspace_size(int64_t nnz, int32_t n_parts);
+
+/*
+ * Read the device status word at the start of a sparse workspace: waits for
+ * `stream`, copies the word to *status.  Returns ZR_ERR_CUDA if the copy
+ * fails, ZR_ERR_INVALID_ARG for NULL pointers, else ZR_OK.
+ */
+zr_status zr_query_status(const void* ws, void* stream, int32_t* status);
+
+/* Static English description of a status code (never NULL). */
+const char* zr_status_string(zr_status s);
+
+/* Library version string, e.g. "zr 0.1.0 sm_103a". */
+const char* zr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZR_H */

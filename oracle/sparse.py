@@ -19,7 +19,9 @@ Test infrastructure only.
   used here: Dietzfelbinger's multiply-add-shift family on 32-bit keys,
   h(x) = ((a*x + b) mod 2**64) >> 32 with a odd and (a, b) drawn from the
   partition seed by SplitMix64, then range reduction
-  p(x) = floor(h(x) * n / 2**32).
+  p(x) = floor(h(x) * n / 2**32).  The key x is the index's 32-bit pattern
+  (indices of a sparse list are non-negative; a push-side list handed to the
+  partition alone may hold any int32).
 * Output order: Algorithm 1 says the order inside a partition does not
   matter; a canonical one is chosen: partition-major, and inside each
   partition the order of the input (ascending index for a union or any
@@ -94,7 +96,7 @@ def union_sort(idx_lists, val_lists, average=False):
 def h0(idx, n_parts, seed):
     """Partition of each index: floor(h(x) * n / 2**32), h multiply-add-shift."""
     a, b = splitmix.h0_params(seed)
-    x = np.asarray(idx, dtype=np.int64).astype(np.uint64)
+    x = (np.asarray(idx, dtype=np.int64) & 0xFFFFFFFF).astype(np.uint64)
     h = (np.uint64(a) * x + np.uint64(b)) >> np.uint64(32)
     return ((h * np.uint64(n_parts)) >> np.uint64(32)).astype(np.int64)
 
@@ -102,7 +104,7 @@ def h0(idx, n_parts, seed):
 def h0_scalar(x, n_parts, seed):
     """The same map on one index, with Python integers."""
     a, b = splitmix.h0_params(seed)
-    h = ((a * int(x) + b) & splitmix.MASK64) >> 32
+    h = ((a * (int(x) & 0xFFFFFFFF) + b) & splitmix.MASK64) >> 32
     return (h * n_parts) >> 32
 
 

@@ -1,0 +1,123 @@
+"""The C-ABI library builds, loads and exports every entry point declared in
+include/*.h; argument checks that return before any CUDA call behave as the
+header documents.  CPU only: no compute call is made here."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def zr():
+    from gradient_synchronisation_gb300 import _build
+
+    _build.build()
+    import gradient_synchronisation_gb300 as zr
+
+    return zr
+
+
+def declared_symbols():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names += re.findall(r"^\s*(?:zr_status|size_t|const char\s*\*)\s*(zr_\w+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_four_operations():
+    names = declared_symbols()
+    for op in ("zr_ring_allreduce", "zr_skipreduce", "zr_sparse_aggregate", "zr_partition"):
+        assert op in names
+
+
+def test_library_exports_every_declared_symbol(zr):
+    lib = ctypes.CDLL(zr.LIB_PATH)
+    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(declared_symbols()) <= set(zr.EXPORTS)
+
+
+def test_binding_has_no_cpu_path():
+    src = open(os.path.join(ROOT, "gradient_synchronisation_gb300", "__init__.py")).read()
+    assert "oracle" not in src
+    for f in glob.glob(os.path.join(ROOT, "gradient_synchronisation_gb300", "**", "*"), recursive=True):
+        if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+            assert "import oracle" not in open(f).read() and "from oracle" not in open(f).read(), f
+
+
+def test_status_strings_and_version(zr):
+    assert zr.status_string(zr.ZR_OK) == "ok"
+    for code in range(8):
+        assert zr.status_string(code)
+    assert "sm_103a" in zr.version()
+
+
+def test_workspace_sizes(zr):
+    assert zr.zr_sparse_workspace_size(0, 100, 4) == 0
+    assert zr.zr_sparse_workspace_size(8, 0, 4) == 0
+    assert zr.zr_sparse_workspace_size(8, 100, -1) == 0
+    assert zr.zr_sparse_workspace_size(8, 100, zr.ZR_MAX_PARTS + 1) == 0
+    a = zr.zr_sparse_workspace_size(8, 1 << 25, 8)
+    b = zr.zr_sparse_workspace_size(8, 1 << 25, 16)
+    assert 0 < a < b and a % 256 == 0
+    assert zr.zr_partition_workspace_size(1000, 0) == 0
+    assert zr.zr_partition_workspace_size(1000, 8) > 0
+
+
+def test_dense_argument_errors_before_launch(zr):
+    fake = [1 << 40, (1 << 40) + (1 << 30)]
+    assert zr.zr_ring_allreduce(fake, 0, 16, zr.ZR_F32, 1, None) == zr.ZR_ERR_INVALID_ARG
+    assert zr.zr_ring_allreduce(fake, 65, 16, zr.ZR_F32, 1, None) == zr.ZR_ERR_INVALID_ARG
+    assert zr.zr_ring_allreduce(fake, 2, -1, zr.ZR_F32, 1, None) == zr.ZR_ERR_INVALID_ARG
+    assert zr.zr_ring_allreduce(fake, 2, 16, 7, 1, None) == zr.ZR_ERR_INVALID_ARG
+    assert zr.zr_ring_allreduce(fake, 2, 16, zr.ZR_F32, 2, None) == zr.ZR_ERR_INVALID_ARG
+    assert zr.zr_ring_allreduce([fake[0] + 4, fake[1]], 2, 16, zr.ZR_F32, 1, None) == zr.ZR_ERR_ALIGNMENT
+    assert zr.zr_ring_allreduce([fake[0], fake[0] + 32], 2, 16, zr.ZR_F32, 1, None) == zr.ZR_ERR_INVALID_ARG
+    assert zr.zr_ring_allreduce([fake[0], 0], 2, 16, zr.ZR_F32, 1, None) == zr.ZR_ERR_INVALID_ARG
+    # m == 0 is a valid no-op (nothing to launch)
+    assert zr.zr_ring_allreduce(fake, 2, 0, zr.ZR_F32, 1, None) == zr.ZR_OK
+    for k in (-1, 2):
+        cfg = zr.SkipCfg(zr.ZR_SKIP_STATIC, k, 0, 0, zr.ZR_DIV_N, 0)
+        assert zr.zr_skipreduce(fake, 2, 16, zr.ZR_F32, cfg, None) == zr.ZR_ERR_INVALID_ARG
+    for bad in (zr.SkipCfg(5, 1, 0, 0, zr.ZR_DIV_N, 0), zr.SkipCfg(0, 1, 0, 0, 9, 0),
+                zr.SkipCfg(0, 1, 0, 0, zr.ZR_DIV_N, 1)):
+        assert zr.zr_skipreduce(fake, 2, 16, zr.ZR_F32, bad, None) == zr.ZR_ERR_INVALID_ARG
+
+
+def test_sparse_argument_errors_before_launch(zr):
+    p = 1 << 40
+    ws = zr.zr_sparse_workspace_size(2, 1000, 4)
+    call = lambda **kw: zr.zr_sparse_aggregate(  # noqa: E731
+        kw.get("idx", [p, p]), kw.get("val", [p, p]), kw.get("nnz", [3, 4]), kw.get("n", 2),
+        kw.get("m", 1000), kw.get("parts", 4), 0, kw.get("avg", 0), p, p, kw.get("cap", 7), p, p,
+        kw.get("ws", p), kw.get("ws_bytes", ws), None)
+    assert call(n=0) == zr.ZR_ERR_INVALID_ARG
+    assert call(m=0) == zr.ZR_ERR_INVALID_ARG
+    assert call(m=1 << 31) == zr.ZR_ERR_INVALID_ARG
+    assert call(parts=zr.ZR_MAX_PARTS + 1) == zr.ZR_ERR_INVALID_ARG
+    assert call(avg=3) == zr.ZR_ERR_INVALID_ARG
+    assert call(nnz=[3, -1]) == zr.ZR_ERR_INVALID_ARG
+    assert call(idx=[p, 0]) == zr.ZR_ERR_INVALID_ARG
+    assert call(cap=6) == zr.ZR_ERR_CAPACITY
+    assert call(ws_bytes=ws - 1) == zr.ZR_ERR_CAPACITY
+    assert call(ws=p + 8) == zr.ZR_ERR_ALIGNMENT
+    assert call(ws=0) == zr.ZR_ERR_INVALID_ARG
+    assert zr.zr_partition(p, p, 10, 0, 0, p, p, p, p, 1 << 20, None) == zr.ZR_ERR_INVALID_ARG
+    assert zr.zr_partition(p, p, -1, 4, 0, p, p, p, p, 1 << 20, None) == zr.ZR_ERR_INVALID_ARG
+    assert zr.zr_partition(p, p, 10, 4, 0, p, p, p, p, 1, None) == zr.ZR_ERR_CAPACITY
+
+
+def test_skip_fraction_to_k(zr):
+    assert zr.skip_fraction_to_k(0.5, 8) == 4
+    assert zr.skip_fraction_to_k(0.25, 8) == 2
+    assert zr.skip_fraction_to_k(0.0, 8) == 0
+    with pytest.raises(ValueError):
+        zr.skip_fraction_to_k(0.3, 8)
+    with pytest.raises(ValueError):
+        zr.skip_fraction_to_k(1.0, 8)
