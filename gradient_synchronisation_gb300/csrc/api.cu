@@ -116,7 +116,8 @@ zr_status zr_sparse_aggregate(const int32_t* const* idx, const float* const* val
   zr_status st = zr::check_ws(ws, ws_bytes, zr::sparse_workspace_bytes(n, dense_size, n_parts));
   if (st != ZR_OK) return st;
   return zr::sparse_launch(idx, val, nnz, n, dense_size, n_parts, part_seed, average, out_idx,
-                           out_val, d_out_nnz, d_offsets, ws, static_cast<cudaStream_t>(stream));
+                           out_val, out_cap, d_out_nnz, d_offsets, ws,
+                           static_cast<cudaStream_t>(stream));
 }
 
 size_t zr_partition_workspace_size(int64_t nnz, int32_t n_parts) {

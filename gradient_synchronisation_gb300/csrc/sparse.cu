@@ -240,7 +240,7 @@ scan_kernel(const int32_t* counts, int64_t bins, int parts, int64_t* pos,
 __global__ void __launch_bounds__(kThreads)
 bin_write_kernel(const __grid_constant__ Lists lists, int n, int64_t bins, const int32_t* starts,
                  H0 h, int parts, int average, const int64_t* pos, int32_t* out_idx,
-                 float* out_val, int32_t* status) {
+                 float* out_val, int64_t out_cap, int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem[];
   float* acc = reinterpret_cast<float*>(smem);                                  // kW
   uint32_t* bits = reinterpret_cast<uint32_t*>(smem + kW * sizeof(float));     // kWords
@@ -280,6 +280,7 @@ bin_write_kernel(const __grid_constant__ Lists lists, int n, int64_t bins, const
       const int p = present ? (parts > 1 ? (int)h(key) : 0) : parts;
       const unsigned peers = __match_any_sync(0xffffffffu, p);
       if (present && (peers & lanemask_lt()) == 0) wbase[warp * parts + p] += __popc(peers);
+      __syncwarp();
     }
     __syncthreads();
     // Exclusive scan over warps, per partition, from the bin's base position.
@@ -304,8 +305,12 @@ bin_write_kernel(const __grid_constant__ Lists lists, int n, int64_t bins, const
         const long long dst = wbase[warp * parts + p] + __popc(peers & lanemask_lt());
         float v = acc[slot];
         if (average) v = __fdiv_rn(v, fn);
-        out_idx[dst] = (int32_t)key;
-        out_val[dst] = v;
+        if (dst >= 0 && dst < out_cap) {  // only malformed input can fail this
+          out_idx[dst] = (int32_t)key;
+          out_val[dst] = v;
+        } else {
+          flag(status, ZR_ERR_INPUT_UNSORTED);
+        }
       }
       __syncwarp();
       if (present && (peers & lanemask_lt()) == 0) wbase[warp * parts + p] += __popc(peers);
@@ -357,6 +362,7 @@ part_write_kernel(const int32_t* idx, const float* val, int64_t nnz, int64_t til
       const int p = live ? (int)h((uint32_t)idx[i]) : parts;
       const unsigned peers = __match_any_sync(0xffffffffu, p);
       if (live && (peers & lanemask_lt()) == 0) wbase[warp * parts + p] += __popc(peers);
+      __syncwarp();
     }
     __syncthreads();
     for (int q = threadIdx.x; q < parts; q += kPartThreads) {
@@ -419,8 +425,8 @@ size_t sparse_workspace_bytes(int n, int64_t dense_size, int n_parts) {
 
 zr_status sparse_launch(const int32_t* const* idx, const float* const* val, const int64_t* nnz,
                         int n, int64_t dense_size, int n_parts, uint64_t part_seed, int average,
-                        int32_t* out_idx, float* out_val, int64_t* d_out_nnz, int64_t* d_offsets,
-                        void* ws, cudaStream_t stream) {
+                        int32_t* out_idx, float* out_val, int64_t out_cap, int64_t* d_out_nnz,
+                        int64_t* d_offsets, void* ws, cudaStream_t stream) {
   const int64_t bins = (dense_size + kW - 1) / kW;
   const int parts = n_parts > 0 ? n_parts : 1;
   const SparseLayout L = sparse_layout(n, bins, parts);
@@ -456,7 +462,7 @@ zr_status sparse_launch(const int32_t* const* idx, const float* const* val, cons
   scan_kernel<<<1, kScanThreads, 0, stream>>>(counts, bins, parts, pos, d_offsets,
                                                (n_parts > 0 && d_offsets) ? 1 : 0, d_out_nnz);
   bin_write_kernel<<<(unsigned)clamp_grid(bins, 4), kThreads, write_smem_bytes(parts), stream>>>(
-      lists, n, bins, starts, h, parts, average, pos, out_idx, out_val, status);
+      lists, n, bins, starts, h, parts, average, pos, out_idx, out_val, out_cap, status);
   return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
 }
 

@@ -21,8 +21,8 @@ zr_status ring_launch(void* const* bufs, int n, int64_t m, zr_dtype dt, int k, i
 size_t sparse_workspace_bytes(int n, int64_t dense_size, int n_parts);
 zr_status sparse_launch(const int32_t* const* idx, const float* const* val, const int64_t* nnz,
                         int n, int64_t dense_size, int n_parts, uint64_t part_seed, int average,
-                        int32_t* out_idx, float* out_val, int64_t* d_out_nnz, int64_t* d_offsets,
-                        void* ws, cudaStream_t stream);
+                        int32_t* out_idx, float* out_val, int64_t out_cap, int64_t* d_out_nnz,
+                        int64_t* d_offsets, void* ws, cudaStream_t stream);
 
 // Push-side partition; arguments already validated.
 size_t partition_workspace_bytes(int64_t nnz, int n_parts);
