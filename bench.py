@@ -61,6 +61,13 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=("ring", "skip", "sparse", "partition"), default=None,
+                    help="profiling: time one component alone (prints a profiling line, not the "
+                         "benchmark line)")
+    ap.add_argument("--dense-m", type=int, default=None,
+                    help="profiling: elements per rank of the dense component (default C2's)")
+    ap.add_argument("--sparse", choices=("c4", "c5b"), default="c4",
+                    help="profiling: sparse workload for --only sparse/partition")
     return ap.parse_args()
 
 
@@ -149,98 +156,107 @@ def summarize_clocks(lines):
 
 
 # ---------------------------------------------------------------- workload
-class Workload:
-    """Device-resident inputs and outputs of one step."""
+COMPONENTS = ("ring", "skip", "sparse", "partition")
 
-    def __init__(self, torch, zr, dev):
+
+class Workload:
+    """Device-resident inputs and outputs of one step (or of one component
+    when profiling with --only)."""
+
+    def __init__(self, torch, zr, dev, only=None, dense_m=None, sparse="c4"):
         import numpy as np
 
         import workloads
 
         self.torch, self.zr, self.dev = torch, zr, dev
+        self.components = (only,) if only else COMPONENTS
         c2 = workloads.DENSE_C2
-        self.n, self.m, self.k = c2["n"], c2["m"], c2["skip_k"]
+        self.n, self.k = c2["n"], c2["skip_k"]
+        self.m = dense_m or c2["m"]
         self.seed = c2["skip_seed"]
-        self.host_dense = workloads.dense_c2()
-        self.dense = torch.from_numpy(self.host_dense).to(dev)
-        self.bufs = [self.dense[r] for r in range(self.n)]
-        c4 = workloads.SPARSE_C4
-        self.m4, self.parts = c4["m"], c4["n_parts"]
-        self.part_seed = c4["part_seed"]
-        idx_l, val_l = workloads.sparse_c4()
-        self.host_idx = [np.ascontiguousarray(a) for a in idx_l]
-        self.host_val = [np.ascontiguousarray(v) for v in val_l]
-        self.d_idx = [torch.from_numpy(a).to(dev) for a in self.host_idx]
-        self.d_val = [torch.from_numpy(v).to(dev) for v in self.host_val]
-        self.nnz = [int(a.size) for a in self.host_idx]
-        self.work = zr.SparseWorkspace(self.n, self.m4, self.parts, sum(self.nnz), dev)
-        self.p_out_idx = torch.empty(self.nnz[0], dtype=torch.int32, device=dev)
-        self.p_out_val = torch.empty(self.nnz[0], dtype=torch.float32, device=dev)
-        self.p_off = torch.empty(self.parts + 1, dtype=torch.int64, device=dev)
-        self.p_ws = torch.empty(zr.zr_partition_workspace_size(self.nnz[0], self.parts),
-                                dtype=torch.uint8, device=dev)
-        # Union size of C4 (fixed by the inputs): run once and read it.
-        zr.sparse_aggregate(self.d_idx, self.d_val, self.m4, self.parts, self.part_seed,
-                            work=self.work)
-        torch.cuda.synchronize()
-        self.union = int(self.work.out_nnz.item())
+        self.dense_on = any(c in self.components for c in ("ring", "skip"))
+        self.sparse_on = any(c in self.components for c in ("sparse", "partition"))
+        if self.dense_on:
+            if dense_m:
+                self.host_dense = workloads.dense_f32_per_rank(self.n, self.m, c2["sigma"], 200)
+            else:
+                self.host_dense = workloads.dense_c2()
+            self.dense = torch.from_numpy(self.host_dense).to(dev)
+            self.bufs = [self.dense[r] for r in range(self.n)]
+        if self.sparse_on:
+            cfg = workloads.SPARSE_C4 if sparse == "c4" else workloads.DGC_C5B
+            self.m4, self.parts = cfg["m"], cfg["n_parts"]
+            self.part_seed = cfg["part_seed"]
+            idx_l, val_l = workloads.sparse_c4() if sparse == "c4" else workloads.dgc_c5b()
+            self.sn = len(idx_l)
+            self.host_idx = [np.ascontiguousarray(a) for a in idx_l]
+            self.host_val = [np.ascontiguousarray(v) for v in val_l]
+            self.d_idx = [torch.from_numpy(a).to(dev) for a in self.host_idx]
+            self.d_val = [torch.from_numpy(v).to(dev) for v in self.host_val]
+            self.nnz = [int(a.size) for a in self.host_idx]
+            self.work = zr.SparseWorkspace(self.sn, self.m4, self.parts, sum(self.nnz), dev)
+            self.p_out_idx = torch.empty(self.nnz[0], dtype=torch.int32, device=dev)
+            self.p_out_val = torch.empty(self.nnz[0], dtype=torch.float32, device=dev)
+            self.p_off = torch.empty(self.parts + 1, dtype=torch.int64, device=dev)
+            self.p_ws = torch.empty(zr.zr_partition_workspace_size(self.nnz[0], self.parts),
+                                    dtype=torch.uint8, device=dev)
+            # The union size is fixed by the inputs: run once and read it.
+            zr.sparse_aggregate(self.d_idx, self.d_val, self.m4, self.parts, self.part_seed,
+                                work=self.work)
+            torch.cuda.synchronize()
+            self.union = int(self.work.out_nnz.item())
 
     def bytes(self):
         s = 4
-        dense_plain = 2 * self.n * self.m * s
-        dense_skip = (self.n - self.k) * self.m * s + self.n * self.m * s
-        sparse = sum(self.nnz) * 8 + self.union * 8 + (self.parts + 1) * 8 + 8
-        part = self.nnz[0] * 8 * 2 + (self.parts + 1) * 8
-        return {"dense_plain": dense_plain, "dense_skip": dense_skip, "sparse": sparse,
-                "partition": part}
+        out = {}
+        if self.dense_on:
+            out["ring"] = 2 * self.n * self.m * s
+            out["skip"] = (self.n - self.k) * self.m * s + self.n * self.m * s
+        if self.sparse_on:
+            out["sparse"] = sum(self.nnz) * 8 + self.union * 8 + (self.parts + 1) * 8 + 8
+            out["partition"] = self.nnz[0] * 8 * 2 + (self.parts + 1) * 8
+        return {c: out[c] for c in self.components}
+
+    def run(self, name, i):
+        zr = self.zr
+        if name == "ring":
+            zr.ring_allreduce(self.bufs, average=True)
+        elif name == "skip":
+            zr.skipreduce(self.bufs, k=self.k, mode=zr.ZR_SKIP_RANDOM, seed=self.seed, step=i)
+        elif name == "sparse":
+            zr.sparse_aggregate(self.d_idx, self.d_val, self.m4, self.parts, self.part_seed,
+                                work=self.work)
+        else:
+            zr.partition(self.d_idx[0], self.d_val[0], self.parts, self.part_seed,
+                         self.p_out_idx, self.p_out_val, self.p_off, self.p_ws)
 
     def step(self, i, events=None):
-        zr = self.zr
-        ev = events or {}
-        if "ring" in ev:
-            ev["ring"][0].record()
-        zr.ring_allreduce(self.bufs, average=True)
-        if "ring" in ev:
-            ev["ring"][1].record()
-        zr.skipreduce(self.bufs, k=self.k, mode=zr.ZR_SKIP_RANDOM, seed=self.seed, step=i)
-        if "skip" in ev:
-            ev["skip"][1].record()
-        zr.sparse_aggregate(self.d_idx, self.d_val, self.m4, self.parts, self.part_seed,
-                            work=self.work)
-        if "sparse" in ev:
-            ev["sparse"][1].record()
-        zr.partition(self.d_idx[0], self.d_val[0], self.parts, self.part_seed, self.p_out_idx,
-                     self.p_out_val, self.p_off, self.p_ws)
-        if "partition" in ev:
-            ev["partition"][1].record()
+        """One pass; ``events`` maps component -> its end event (recorded on
+        the current stream, the one every call is launched on)."""
+        for name in self.components:
+            self.run(name, i)
+            if events is not None:
+                events[name].record()
 
 
 def timed_device(torch, W, steps, warmup):
     for i in range(warmup):
         W.step(i)
     torch.cuda.synchronize()
-    names = ("ring", "skip", "sparse", "partition")
-    per = {n: [] for n in names}
+    names = W.components
     start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    evs = []
-    for i in range(steps):
-        e = {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for n in names}
-        # each component starts where the previous one ended
-        e["skip"] = (e["ring"][1], e["skip"][1])
-        e["sparse"] = (e["skip"][1], e["sparse"][1])
-        e["partition"] = (e["sparse"][1], e["partition"][1])
-        evs.append(e)
+    evs = [{n: torch.cuda.Event(enable_timing=True) for n in names} for _ in range(steps)]
     start.record()
     for i in range(steps):
         W.step(warmup + i, evs[i])
-    stop.record()
     torch.cuda.synchronize()
-    total_ms = start.elapsed_time(stop)
+    total_ms = start.elapsed_time(evs[-1][names[-1]])
+    per = {n: [] for n in names}
+    prev = start
     for e in evs:
         for n in names:
-            per[n].append(e[n][0].elapsed_time(e[n][1]))
+            per[n].append(prev.elapsed_time(e[n]))  # each component starts where the last ended
+            prev = e[n]
     return total_ms, per
 
 
@@ -379,7 +395,7 @@ def main():
     __graft_entry__.build()
     import gradient_synchronisation_gb300 as zr
 
-    W = Workload(torch, zr, dev)
+    W = Workload(torch, zr, dev, only=args.only, dense_m=args.dense_m, sparse=args.sparse)
     b = W.bytes()
     step_bytes = sum(b.values())
 
@@ -399,19 +415,27 @@ def main():
 
     value = world * step_bytes * args.steps / (total_ms / 1e3) / 1e9
     peak, peak_kind = measured_hbm()
-    ring_ms = statistics.mean(per["ring"] + per["skip"])
-    ring_bytes = (b["dense_plain"] + b["dense_skip"]) / 2
-    achieved = ring_bytes / (ring_ms / 1e3) / 1e9
+    parts = {}
+    for name in W.components:
+        ms = statistics.median(per[name])
+        parts[name] = {"bytes": b[name], "median_ms": ms, "gbs": b[name] / (ms / 1e3) / 1e9,
+                       "frac": b[name] / (ms / 1e3) / 1e9 / peak}
+    if args.only:
+        if rank == 0:
+            print(json.dumps({"profiling": args.only, "dense_m": W.m if W.dense_on else None,
+                              "sparse": args.sparse if W.sparse_on else None,
+                              "steps": args.steps, "parts": parts, "peak": peak}))
+        return 0
+
+    # Dominant kernel: ring_fused_kernel<float>.  achieved = the algorithmic
+    # bytes of its plain all-reduce launch (2*N*M*4) over that launch's mean
+    # CUDA-event duration; the SkipReduce launch of the same kernel is in
+    # parts["skip"].
+    ring_ms = statistics.mean(per["ring"])
+    achieved = b["ring"] / (ring_ms / 1e3) / 1e9
     tr = TRAFFIC["ring_fused_kernel<float>"]
     sha = source_sha(os.path.join(ROOT, "gradient_synchronisation_gb300", "csrc", "ring.cu"))
     traffic = tr["bytes_per_launch"] if tr["source_sha256"] == sha else None
-
-    parts = {}
-    for name, key in (("ring", "dense_plain"), ("skip", "dense_skip"), ("sparse", "sparse"),
-                      ("partition", "partition")):
-        ms = statistics.median(per[name])
-        parts[name] = {"bytes": b[key], "median_ms": ms, "gbs": b[key] / (ms / 1e3) / 1e9,
-                       "frac": b[key] / (ms / 1e3) / 1e9 / peak}
 
     e2e = None
     if not args.no_e2e:
@@ -435,7 +459,7 @@ def main():
                        "parallelism": "replicas only" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "ring_fused_kernel<float> (C2 plain + SkipReduce launches)",
+                         "kernel": "ring_fused_kernel<float>, C2 plain all-reduce launch",
                          "peak_source": peak_kind},
             "parts": parts,
             "e2e": e2e,
