@@ -50,7 +50,7 @@ TRAFFIC = {
 }
 
 # Kernel launches each library call makes (counted from the library source).
-LAUNCHES = {"ring": 1, "skip": 1, "sparse": 4, "partition": 3}
+LAUNCHES = {"ring": 1, "skip": 1, "sparse": 3, "partition": 2}
 
 
 def parse():
