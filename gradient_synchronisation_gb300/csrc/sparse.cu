@@ -275,8 +275,9 @@ union_count_kernel(const __grid_constant__ Lists lists, int n, int64_t dense_siz
   __shared__ int64_t lo_s[ZR_MAX_RANKS], hi_s[ZR_MAX_RANKS];
   __shared__ int64_t s_bin;
   __shared__ int s_flag;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t W = 1ll << log_w;
+  const H0 hash = h;
   for (;;) {
     if (tid == 0) s_bin = atomicAdd(ticket, 1u);
     __syncthreads();
@@ -299,13 +300,24 @@ union_count_kernel(const __grid_constant__ Lists lists, int n, int64_t dense_siz
       }
     }
     __syncthreads();
-    for (int w = tid; w < words; w += kThreads) {
-      uint32_t bits = ubits[w];
-      while (bits) {
-        const int bit = __ffs(bits) - 1;
-        bits &= bits - 1;
-        const uint32_t key = (uint32_t)(base + w * 32 + bit);
-        atomicAdd(&cnt[parts > 1 ? (int)h(key) : 0], 1);
+    // Count the union members per partition, a warp per 32-word window;
+    // lanes are mapped to members by a warp-level load-balancing search.
+    for (int c = warp * 32; c < words; c += kWarps * 32) {
+      const uint32_t wbits = ubits[c + lane];
+      const int cntl = __popc(wbits);
+      const int incl_l = warp_incl_scan(cntl);
+      const int total = __shfl_sync(0xffffffffu, incl_l, 31);
+      for (int q = 0; q < total; q += 32) {
+        const int j = q + lane;
+        const bool live = j < total;
+        const int o = owner_lane(incl_l, j);
+        const uint32_t ow = __shfl_sync(0xffffffffu, wbits, o);
+        const int oex = __shfl_sync(0xffffffffu, incl_l - cntl, o);
+        const int bit = live ? select_bit(ow, j - oex) : 0;
+        const uint32_t key = (uint32_t)(base + (c + o) * 32 + bit);
+        const int p = live ? (parts > 1 ? (int)hash(key) : 0) : parts;
+        const unsigned peers = __match_any_sync(0xffffffffu, p);
+        if (live && (peers & lanemask_lt()) == 0) atomicAdd(&cnt[p], __popc(peers));
       }
     }
     __syncthreads();
@@ -367,6 +379,7 @@ union_write_kernel(const __grid_constant__ Lists lists, int n, int log_w, int wo
   const int per_warp = words / kWarps;  // >= 8
   const int win = per_warp < 32 ? per_warp : 32;
   const float fn = (float)n;
+  const H0 hash = h;
 
   for (int64_t b = blockIdx.x; b < bins; b += gridDim.x) {
     const int64_t base = b << log_w;
@@ -431,7 +444,7 @@ union_write_kernel(const __grid_constant__ Lists lists, int n, int log_w, int wo
           const int bit = live ? select_bit(ow, j - oex) : 0;
           const int wd = c + o;
           const uint32_t key = (uint32_t)(base + wd * 32 + bit);
-          const int p = live ? (parts > 1 ? (int)h(key) : 0) : parts;
+          const int p = live ? (parts > 1 ? (int)hash(key) : 0) : parts;
           const unsigned peers = __match_any_sync(0xffffffffu, p);
           const bool leader = live && (peers & lanemask_lt()) == 0;
           if (pass == 1 && live) {
@@ -501,6 +514,7 @@ part_count_kernel(const int32_t* idx, int64_t nnz, int64_t tiles, H0 h, int part
   __shared__ int64_t s_tile;
   __shared__ int s_flag;
   const int tid = threadIdx.x;
+  const H0 hash = h;
   for (;;) {
     if (tid == 0) s_tile = atomicAdd(ticket, 1u);
     for (int q = tid; q < parts; q += kPartThreads) cnt[q] = 0;
@@ -510,7 +524,7 @@ part_count_kernel(const int32_t* idx, int64_t nnz, int64_t tiles, H0 h, int part
     const int64_t lo = t * kPartTile, hi = min(lo + kPartTile, nnz);
     for (int64_t i = lo + tid; i < lo + kPartTile; i += kPartThreads) {
       const bool live = i < hi;
-      const int p = live ? (int)h((uint32_t)idx[i]) : parts;
+      const int p = live ? (int)hash((uint32_t)idx[i]) : parts;
       const unsigned peers = __match_any_sync(0xffffffffu, p);
       if (live && (peers & lanemask_lt()) == 0) atomicAdd(&cnt[p], __popc(peers));
     }
@@ -532,6 +546,7 @@ part_write_kernel(const int32_t* idx, const float* val, int64_t nnz, int64_t til
   constexpr int kPW = kPartThreads / 32;
   constexpr int kPerWarp = kPartTile / kPW;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const H0 hash = h;
   for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
     for (int q = threadIdx.x; q < kPW * parts; q += kPartThreads) wbase[q] = 0;
     __syncthreads();
@@ -540,7 +555,7 @@ part_write_kernel(const int32_t* idx, const float* val, int64_t nnz, int64_t til
     for (int j = 0; j < kPerWarp; j += 32) {
       const int64_t i = lo + j + lane;
       const bool live = i < hi;
-      const int p = live ? (int)h((uint32_t)idx[i]) : parts;
+      const int p = live ? (int)hash((uint32_t)idx[i]) : parts;
       const unsigned peers = __match_any_sync(0xffffffffu, p);
       if (live && (peers & lanemask_lt()) == 0) wbase[warp * parts + p] += __popc(peers);
       __syncwarp();
@@ -559,7 +574,7 @@ part_write_kernel(const int32_t* idx, const float* val, int64_t nnz, int64_t til
       const int64_t i = lo + j + lane;
       const bool live = i < hi;
       const int32_t key = live ? idx[i] : 0;
-      const int p = live ? (int)h((uint32_t)key) : parts;
+      const int p = live ? (int)hash((uint32_t)key) : parts;
       const unsigned peers = __match_any_sync(0xffffffffu, p);
       if (live) {
         const long long dst = wbase[warp * parts + p] + __popc(peers & lanemask_lt());
