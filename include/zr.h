@@ -183,8 +183,7 @@ size_t zr_sparse_workspace_size(int32_t n, int64_t dense_size, int32_t n_parts);
  *            unique).  out_idx, out_val: device outputs of nnz entries.
  * d_offsets  device int64[n_parts + 1].   1 <= n_parts <= ZR_MAX_PARTS.
  * ws         device workspace of zr_partition_workspace_size(nnz, n_parts)
- *            bytes, 16-byte aligned.  Its first 4 bytes are the status word
- *            (ZR_ERR_TIMEOUT if a bounded wait between CTAs gave up).
+ *            bytes, 16-byte aligned.
  * Result: entries grouped by p(idx) (same h0 as above), partition-major; inside
  * a partition entries keep their input order (a stable split).
  */

@@ -93,6 +93,19 @@ def test_edge_cases(env):
     assert np.array_equal(gv[ok].view(np.uint32), wv[ok].view(np.uint32))
 
 
+def test_wide_key_range_many_partitions(env):
+    # A dense size large enough that the per-warp partition counts do not
+    # fit their workspace budget, so the writer recounts them itself.
+    torch, zr = env
+    rng = np.random.default_rng(12)
+    m = 1 << 27
+    idx_l = [np.unique(rng.integers(0, m, size=3000)).astype(np.int32) for _ in range(3)]
+    idx_l[1] = np.union1d(idx_l[1], idx_l[0][::3]).astype(np.int32)
+    val_l = [rng.standard_normal(a.size).astype(np.float32) for a in idx_l]
+    for n_parts in (256, 3, 0):
+        check(torch, zr, idx_l, val_l, m, n_parts, seed=1)
+
+
 def test_unsorted_input_sets_status(env):
     torch, zr = env
     good = np.array([1, 5, 9], np.int32)
