@@ -93,6 +93,21 @@ def source_sha(path):
         return hashlib.sha256(f.read()).hexdigest()
 
 
+# ---------------------------------------------------------------- timing
+def max_over_ranks(ms, dist_mod, device):
+    """The slowest rank's time (all_reduce MAX; a timing collective only)."""
+    import torch
+
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(step_bytes, steps, world, max_ms):
+    """Whole-job GB/s: every replica processed step_bytes per step."""
+    return world * step_bytes * steps / (max_ms / 1e3) / 1e9
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples (every 200 ms) while the timed region runs."""
@@ -407,13 +422,11 @@ def main():
     total_ms, per = timed_device(torch, W, args.steps, args.warmup)
     clk = clocks.stop()
     if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dist, dev)
         dist.barrier()
     torch.cuda.synchronize()
 
-    value = world * step_bytes * args.steps / (total_ms / 1e3) / 1e9
+    value = job_throughput(step_bytes, args.steps, world, total_ms)
     peak, peak_kind = measured_hbm()
     parts = {}
     for name in W.components:
