@@ -49,8 +49,9 @@ ZR_MAX_PARTS = 256
 EXPORTS = (
     "zr_ring_allreduce", "zr_skipreduce", "zr_sparse_aggregate", "zr_sparse_workspace_size",
     "zr_partition", "zr_partition_workspace_size", "zr_query_status", "zr_status_string",
-    "zr_version",
+    "zr_version", "zr_partition_static",
 )
+ZR_STATIC_SCRATCH_BYTES = 2 << 20
 
 
 class ZrError(RuntimeError):
@@ -84,6 +85,7 @@ def _load():
         "zr_query_status": (i32, [P, P, ctypes.POINTER(i32)]),
         "zr_status_string": (ctypes.c_char_p, [i32]),
         "zr_version": (ctypes.c_char_p, []),
+        "zr_partition_static": (i32, [P, P, i64, i32, u64, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -135,6 +137,12 @@ def zr_partition(idx, val, nnz, n_parts, part_seed, out_idx, out_val, d_offsets,
                  stream):
     return lib().zr_partition(idx, val, nnz, n_parts, part_seed, out_idx, out_val, d_offsets, ws,
                              ws_bytes, stream)
+
+
+def zr_partition_static(idx, val, nnz, n_parts, part_seed, out_idx, out_val, d_offsets, stream):
+    """zr_partition with the library's own fixed scratch (no workspace)."""
+    return lib().zr_partition_static(idx, val, nnz, n_parts, part_seed, out_idx, out_val,
+                                     d_offsets, stream)
 
 
 def zr_partition_workspace_size(nnz, n_parts):

@@ -196,6 +196,28 @@ zr_status zr_partition(const int32_t* idx, const float* val, int64_t nnz,
 size_t zr_partition_workspace_size(int64_t nnz, int32_t n_parts);
 
 /*
+ * zr_partition without a workspace argument, for callers that cannot
+ * allocate device memory (for example a gradient hook running inside a
+ * framework whose caching allocator owns the device, or a service that
+ * reserves all device memory at start-up).  The pages have no counterpart:
+ * it exists only for such callers.
+ *
+ * Arguments and result are those of zr_partition minus ws / ws_bytes.  The
+ * scratch is a fixed array of ZR_STATIC_SCRATCH_BYTES inside the library on
+ * every device that loads it; a request whose
+ * zr_partition_workspace_size(nnz, n_parts) exceeds that returns
+ * ZR_ERR_CAPACITY and enqueues nothing.  The library never calls cudaMalloc
+ * or cudaFree here.  The first call on a device (with that device current)
+ * looks up the array's device address; make that first call before any
+ * stream capture.  All calls on a device share the array (each call clears
+ * what must start at zero), so calls that overlap on the GPU race.
+ */
+#define ZR_STATIC_SCRATCH_BYTES (2u << 20)
+zr_status zr_partition_static(const int32_t* idx, const float* val, int64_t nnz,
+                              int32_t n_parts, uint64_t part_seed, int32_t* out_idx,
+                              float* out_val, int64_t* d_offsets, void* stream);
+
+/*
  * Read the device status word at the start of a sparse workspace: waits for
  * `stream`, copies the word to *status.  Returns ZR_ERR_CUDA if the copy
  * fails, ZR_ERR_INVALID_ARG for NULL pointers, else ZR_OK.
