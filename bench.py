@@ -46,7 +46,11 @@ WORKLOAD = ("C2 dense ring all-reduce N=8 M=25,557,032 fp32 (plain + Random Skip
 # dram__bytes_write.sum per launch), valid only while the kernel source is the
 # one that was profiled.  The command that produced it is in profiles/.
 TRAFFIC = {
-    "ring_fused_kernel<float>": {"source_sha256": None, "bytes_per_launch": None},
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the full C2
+    # plain launch (profiles/ring_fused_kernel_c2_shape.md): 817.88 MB read
+    # + 760.63 MB written (the rest of the writes still sit in L2 at the end).
+    "ring_fused_kernel<float>": {"source_sha256": "282d38cc1278150742370aeec2014a320a62211d052651ba0a5bf54b8767ea08",
+                                 "bytes_per_launch": 1_578_510_000},
 }
 
 # Kernel launches each library call makes (counted from the library source).
