@@ -35,6 +35,7 @@ ZR_ERR_CAPACITY = 4
 ZR_ERR_INPUT_UNSORTED = 5
 ZR_ERR_TIMEOUT = 6
 ZR_ERR_CUDA = 7
+ZR_ERR_INTERNAL = 8
 
 ZR_F32 = 0
 ZR_BF16 = 1

@@ -156,6 +156,7 @@ const char* zr_status_string(zr_status s) {
     case ZR_ERR_INPUT_UNSORTED: return "sparse indices not strictly ascending or out of range";
     case ZR_ERR_TIMEOUT: return "device wait timed out";
     case ZR_ERR_CUDA: return "CUDA error";
+    case ZR_ERR_INTERNAL: return "internal consistency check failed on the device";
   }
   return "unknown status";
 }

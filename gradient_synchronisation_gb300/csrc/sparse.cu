@@ -6,32 +6,30 @@
 // that hold it, split into n_parts partitions by the consistent hash h0 and
 // written partition-major, ascending index inside a partition.
 //
-// GB300 design.  The key range [0, M) is cut into bins of W keys (W = 16384
-// for up to 8 ranks, halving as the rank count doubles so that the per-rank
-// bitmaps of one bin stay at 16 KB of shared memory).  Work inside a bin is
-// proportional to its entries, not to W:
-//   1. sample:  every 64th index of every list gives, for each rank and bin,
-//      a position at most 63 entries before the bin's first entry (one
-//      32-byte sector in eight of the index bytes is read).
-//   2. count:   per bin, OR the keys of every rank into a W-bit union bitmap
-//      in shared memory (checking that each list is strictly ascending and
-//      in range) and count the union members per partition; per-bin counts
-//      plus atomically summed segment and partition totals give every bin
-//      its output positions without any CTA waiting for another.
-//   3. write:   per bin, build one bitmap per rank and its per-word prefix
-//      counts plus a holder mask per key, stage the bin's values in shared
-//      memory (16-byte loads over all ranks' ranges at once), then walk the union members in ascending key order, a warp
-//      at a time over 32-word windows (a warp-level load-balancing search
-//      maps lanes to members).  Each member gathers its holders' values in
-//      ascending rank order straight from the input lists (the position of a
-//      key in rank r's list is the bin's start plus a bitmap prefix count)
-//      and folds them left from -0.0 (-0.0 + x == x for every x, so this is
-//      exactly "start from the first holder's value").  A warp-level stable
-//      multi-split on the partition id places each member.
+// GB300 design.  The key range [0, M) is cut into bins of W keys (W = 1024,
+// wider only when the workspace would otherwise grow too large).  A bin is
+// the work of one warp, so nothing inside a bin waits on a block barrier,
+// and tens of warps per SM hide each other's memory latency:
+//   1. starts:  one streaming pass over every list (16-byte loads) writes,
+//      for every rank and bin, where the bin's entries start, and checks
+//      that each list is strictly ascending and in range.
+//   2. count:   per bin, a warp ORs the keys of every rank into the bin's
+//      W-bit union bitmap (warp-private shared memory), hashes each member
+//      and counts members per partition.
+//   3. scan:    one CTA per partition turns the per-bin counts into each
+//      bin's first output position in that partition.
+//   4. write:   per bin, a warp streams the bin's entries rank by rank in
+//      groups of up to 32 entries of one rank (the loads of several groups
+//      in flight at once) and folds them into a warp-private W-float window
+//      in ascending rank order: the first holder's value is stored, later
+//      holders are added, which is the left fold of the holders' values.
+//      Then each lane takes one bitmap word (32 keys in order), counts its
+//      members per partition, and after a prefix over lanes the
+//      members are written in ascending key order inside each partition.
 //
 // Every index taken from the inputs is range-checked before it addresses
-// shared memory, segment bounds read from the workspace are clamped to the
-// list lengths, and every output position is checked against the output
+// shared memory, bounds read from the workspace are clamped to the list
+// lengths, and every output position is checked against the output
 // capacity, so malformed input can only produce wrong output and a status
 // word, never an out-of-bounds access.
 
@@ -45,12 +43,11 @@
 namespace zr {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
-constexpr int kSample = 64;              // stride of the sampling pass
-constexpr int kLogW = 13;                // bin width W = 8192 keys
-constexpr int kWords = (1 << kLogW) / 32;  // union bitmap words per bin
-constexpr int kStage = 8192;             // entries of one bin staged in shared memory
+constexpr int kBinWarps = 8;             // warps per CTA in the count and write kernels
+constexpr int kBinThreads = kBinWarps * 32;
+constexpr int kBatch = 8;                // entries per lane per load batch
+constexpr int kWriteWarps = 4;           // warps per CTA in the write kernel
+constexpr int kWriteThreads = kWriteWarps * 32;
 constexpr int kPartTile = 4096;          // zr_partition: entries per tile
 constexpr int kPartThreads = 512;
 
@@ -68,21 +65,6 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   return m;
 }
 
-// Position (0-based) of the n-th set bit of x; x must have more than n bits set.
-__device__ __forceinline__ int select_bit(uint32_t x, int n) {
-  int pos = 0;
-  int c = __popc(x & 0xFFFFu);
-  if (n >= c) { n -= c; x >>= 16; pos += 16; }
-  c = __popc(x & 0xFFu);
-  if (n >= c) { n -= c; x >>= 8; pos += 8; }
-  c = __popc(x & 0xFu);
-  if (n >= c) { n -= c; x >>= 4; pos += 4; }
-  c = __popc(x & 0x3u);
-  if (n >= c) { n -= c; x >>= 2; pos += 2; }
-  if (n >= (int)(x & 1u)) pos += 1;
-  return pos;
-}
-
 __device__ __forceinline__ int warp_incl_scan(int v) {
   const int lane = threadIdx.x & 31;
   for (int o = 1; o < 32; o <<= 1) {
@@ -92,22 +74,10 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
   return v;
 }
 
-// Smallest lane whose inclusive prefix exceeds j (the lanes hold a
-// non-decreasing prefix); every lane searches for its own j.
-__device__ __forceinline__ int owner_lane(int incl, int j) {
-  int pos = 0;
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) {
-    const int v = __shfl_sync(0xffffffffu, incl, pos + s - 1);
-    if (v <= j) pos += s;
-  }
-  return pos;
-}
-
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // ------------------------------------------------------------ positions
-// Output positions come from per-unit (bin or tile) member counts per
+// zr_partition: output positions come from per-tile entry counts per
 // partition, with two order-free sums kept beside them: the totals of every
 // segment of kSeg consecutive units and the grand total per partition, both
 // accumulated with integer atomics.  The first output position of unit u in
@@ -169,422 +139,595 @@ __device__ void unit_base(int64_t u, int parts, const long long* offs, const int
   }
 }
 
+
 // ------------------------------------------------------------ layout
+// Bins are W = 2^log_w keys: 1024, widened (up to 4096) only when the
+// per-(bin, partition) tables would exceed 2^24 entries.
+constexpr int kChunkLog = 11;            // bins per scan chunk = 2048
+constexpr int kChunkBins = 1 << kChunkLog;
+constexpr int kScanThreads = kChunkBins / 2;
+
 struct Geometry {
-  int log_w;   // bin width W = 2^log_w keys
-  int words;   // W / 32
+  int log_w;
   int64_t bins;
 };
 
-// Bins are W = 8192 keys for any rank count: the writer folds a bin into a
-// W-float window in shared memory.
-Geometry geometry(int, int64_t dense_size) {
+Geometry geometry(int n, int64_t dense_size, int parts, int64_t total_nnz) {
   Geometry g;
-  g.log_w = kLogW;
-  g.words = kWords;
-  g.bins = (dense_size + (1ll << kLogW) - 1) >> kLogW;
+  (void)total_nnz;
+  g.log_w = 10;
+  for (;;) {
+    g.bins = (dense_size + (1ll << g.log_w) - 1) >> g.log_w;
+    if (g.log_w >= 12 || g.bins * (int64_t)(parts + n) <= (1ll << 24)) break;
+    ++g.log_w;
+  }
   return g;
 }
 
-// Per-(bin, warp, partition) member counts let the writer place members
-// without recounting them; kept when they fit in 16 MB of workspace.
-bool keep_warp_counts(int64_t bins, int parts) {
-  return (double)bins * kWarps * parts <= (double)(1 << 22);
-}
-
-// [status | totals | segment totals] are contiguous so one memset clears them.
+// Workspace: [status] (cleared by a memset), then the bin starts, the
+// per-bin counts, the per-chunk totals, the per-bin exclusive prefixes and
+// the partition totals.
 struct SparseLayout {
-  size_t tot, seg, coarse, cnt, wcnt, total;
+  size_t starts, cnt, ctot, excl, tot, total;
 };
 
 SparseLayout sparse_layout(int n, int64_t bins, int parts) {
   SparseLayout L;
-  const int64_t segs = (bins + kSeg - 1) >> kSegLog;
-  L.tot = 256;
-  L.seg = L.tot + align256((size_t)parts * 8);
-  L.coarse = L.seg + align256((size_t)segs * parts * 8);
-  L.cnt = L.coarse + align256((size_t)n * (size_t)(bins + 1) * 4);
-  L.wcnt = L.cnt + align256((size_t)bins * parts * 4);
-  L.total = L.wcnt + (keep_warp_counts(bins, parts) ? align256((size_t)bins * kWarps * parts * 4) : 0);
+  const int64_t chunks = (bins + kChunkBins - 1) >> kChunkLog;
+  L.starts = 256;
+  L.cnt = L.starts + align256((size_t)n * (size_t)(bins + 1) * 4);
+  L.ctot = L.cnt + align256((size_t)parts * bins * 4);
+  L.excl = L.ctot + align256((size_t)parts * chunks * 8);
+  L.tot = L.excl + align256((size_t)parts * bins * 8);
+  L.total = L.tot + align256((size_t)parts * 8);
   return L;
 }
 
-// ------------------------------------------------------------ 1. sample
-__device__ __forceinline__ int64_t bin_of(int64_t key, int log_w, int64_t bins) {
+__device__ __forceinline__ int bin_of(int key, int log_w, int bins) {
   return key < 0 ? -1 : min(key >> log_w, bins);
 }
 
-// Grid: x over samples (plus one thread for the end), y = rank.
-// coarse[r][b] = position of the first sample whose bin is >= b (nnz if none).
-__global__ void sample_kernel(const __grid_constant__ Lists lists, int64_t dense_size, int log_w,
-                              int64_t bins, int32_t* coarse, int32_t* status) {
+// ------------------------------------------------------------ 1. starts
+// Grid: x over groups of 4 positions (the last group holds position nnz,
+// the end marker), y = rank.  starts[r][b] = first position whose key is in
+// bin >= b (nnz if none); every list is checked strictly ascending and in
+// range.  32-bit index arithmetic throughout (positions, keys and bins all
+// fit).
+__global__ void __launch_bounds__(256)
+bin_starts_kernel(const __grid_constant__ Lists lists, int dense_size, int log_w, int bins,
+                  int32_t* starts, int32_t* status) {
   const int r = blockIdx.y;
-  const int64_t nnz = lists.nnz[r];
+  const int nnz = (int)lists.nnz[r];
   const int32_t* idx = lists.idx[r];
-  const int64_t samples = (nnz + kSample - 1) / kSample;
-  int32_t* row = coarse + (size_t)r * (bins + 1);
-  for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j <= samples;
-       j += (int64_t)gridDim.x * blockDim.x) {
-    int64_t b_here, at;
-    if (j < samples) {
-      const int64_t key = idx[j * kSample];
-      if (key < 0 || key >= dense_size) flag(status, ZR_ERR_INPUT_UNSORTED);
-      if (j > 0 && key <= (int64_t)idx[(j - 1) * kSample]) flag(status, ZR_ERR_INPUT_UNSORTED);
-      b_here = bin_of(key, log_w, bins);
-      at = j * kSample;
+  int32_t* row = starts + (size_t)r * (bins + 1);
+  const bool vec = (reinterpret_cast<uintptr_t>(idx) & 15) == 0;
+  const int groups = nnz / 4 + 1;
+  for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < groups; q += gridDim.x * blockDim.x) {
+    const int i0 = q * 4;
+    int key[4] = {0, 0, 0, 0};
+    if (vec && i0 + 4 <= nnz) {
+      const int4 k4 = __ldg(reinterpret_cast<const int4*>(idx) + q);
+      key[0] = k4.x; key[1] = k4.y; key[2] = k4.z; key[3] = k4.w;
     } else {
-      b_here = bins;
-      at = nnz;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (i0 + e < nnz) key[e] = __ldg(idx + i0 + e);
     }
-    const int64_t b_prev = j == 0 ? -1 : bin_of(idx[(j - 1) * kSample], log_w, bins);
-    for (int64_t b = b_prev + 1; b <= b_here; ++b) row[b] = (int32_t)at;
+    int prev = i0 > 0 ? __ldg(idx + i0 - 1) : -1;
+    int b_prev = i0 > 0 ? bin_of(prev, log_w, bins) : -1;
+    bool bad = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = i0 + e;
+      if (i > nnz) break;
+      int b_here;
+      if (i < nnz) {
+        const int k = key[e];
+        if (k < 0 || k >= dense_size || (i > 0 && k <= prev)) bad = true;
+        b_here = bin_of(k, log_w, bins);
+        prev = k;
+      } else {
+        b_here = bins;
+      }
+      for (int bb = b_prev + 1; bb <= b_here; ++bb) row[bb] = i;
+      if (b_here > b_prev) b_prev = b_here;
+    }
+    if (bad) flag(status, ZR_ERR_INPUT_UNSORTED);
   }
 }
 
-// Entries of bin b in rank r lie inside [lo, hi).
-__device__ __forceinline__ void bin_range(const int32_t* coarse, int64_t bins, int r, int64_t b,
-                                          int64_t nnz, int64_t& lo, int64_t& hi) {
-  const int32_t* row = coarse + (size_t)r * (bins + 1);
-  lo = min(max((int64_t)row[b] - (kSample - 1), (int64_t)0), nnz);
-  hi = min(max((int64_t)row[b + 1], lo), nnz);
-}
-
-// Walks the union members of the calling warp's words in ascending key
-// order, 32 members at a time, and calls f(live, key, word, bit, p, peers)
-// with every lane of the warp (peers: lanes of the same partition p; p is
-// `parts` for lanes without a member).
-template <typename F>
-__device__ __forceinline__ void for_members(const uint32_t* ubits, int c0, int c1, int64_t base,
-                                            const H0& hash, int parts, F&& f) {
-  const int lane = threadIdx.x & 31;
-  const int win = (c1 - c0) < 32 ? (c1 - c0) : 32;
-  for (int c = c0; c < c1; c += win) {
-    const uint32_t wbits = lane < win ? ubits[c + lane] : 0u;
-    const int cntl = __popc(wbits);
-    const int incl = warp_incl_scan(cntl);
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    for (int q = 0; q < total; q += 32) {
-      const int j = q + lane;
-      const bool live = j < total;
-      const int o = owner_lane(incl, j);
-      const uint32_t ow = __shfl_sync(0xffffffffu, wbits, o);
-      const int oex = __shfl_sync(0xffffffffu, incl - cntl, o);
-      const int bit = live ? select_bit(ow, j - oex) : 0;
-      const int wd = c + o;
-      const uint32_t key = (uint32_t)(base + wd * 32 + bit);
-      const int p = live ? (parts > 1 ? (int)hash(key) : 0) : parts;
-      const unsigned peers = __match_any_sync(0xffffffffu, p);
-      f(live, key, wd, bit, p, peers);
-    }
-  }
-}
-
-// ------------------------------------------------------------ bin entries
-// Where the entries of one bin lie in every rank's list, and how the block
-// walks them: each rank's range [lo, hi) is cut into 16-byte chunks (4
-// entries; when the list is 16-byte aligned) plus at most 3 + 3 single
-// entries at its ends, and the chunks of all ranks are walked as one
-// flattened sequence so that many independent loads are in flight.
-struct BinRanges {
-  int64_t lo[ZR_MAX_RANKS], hi[ZR_MAX_RANKS];
-  int64_t vlo[ZR_MAX_RANKS];           // first chunk (in chunks of 4 entries)
-  int32_t cpre[ZR_MAX_RANKS + 1];      // prefix of chunk counts
-  int32_t spre[ZR_MAX_RANKS + 1];      // prefix of single-entry counts
-  int32_t epre[ZR_MAX_RANKS + 1];      // prefix of range lengths (staging offsets)
+// Per-warp layout of one bin: rank r's entries are positions
+// [lo[r], lo[r] + len) of its list and [epre[r], epre[r+1]) of the bin's
+// rank-major flattened sequence.
+struct BinRanks {
+  int lo[ZR_MAX_RANKS];
+  int epre[ZR_MAX_RANKS + 1];
 };
 
-// Two halves, so that a kernel can issue other independent loads between
-// them: bin_ranges_load (threads r < n read the sampled bounds) and, after a
-// barrier, bin_ranges_finish (thread 0 lays out chunks and singles).
-__device__ __forceinline__ void bin_ranges_load(const Lists& lists, int n, const int32_t* coarse,
-                                                int64_t bins, int64_t b, BinRanges& R) {
-  for (int r = threadIdx.x; r < n; r += blockDim.x) {
-    int64_t lo, hi;
-    bin_range(coarse, bins, r, b, lists.nnz[r], lo, hi);
-    R.lo[r] = lo;
-    R.hi[r] = hi;
-  }
-}
+// A bin's raw start rows for ranks lane and lane + 32, loaded ahead of use
+// so that the next bin's loads are in flight while the current bin works.
+struct BinFetch {
+  int lo[2], hi[2];
+};
 
-__device__ __forceinline__ void bin_ranges_finish(const Lists& lists, int n, BinRanges& R) {
-  if (threadIdx.x == 0) {
-    int32_t c = 0, sgl = 0, e = 0;
-    for (int r = 0; r < n; ++r) {
-      const int64_t lo = R.lo[r], hi = R.hi[r];
-      const bool vec = (reinterpret_cast<uintptr_t>(lists.idx[r]) & 15) == 0 &&
-                       (reinterpret_cast<uintptr_t>(lists.val[r]) & 15) == 0;
-      int64_t vlo = (lo + 3) >> 2, vhi = hi >> 2;
-      if (!vec || vlo > vhi) vlo = vhi = (lo + 3) >> 2;
-      R.vlo[r] = vlo;
-      R.cpre[r] = c;
-      R.spre[r] = sgl;
-      R.epre[r] = e;
-      const int64_t chunks = (vec && vhi > vlo) ? vhi - vlo : 0;
-      c += (int32_t)chunks;
-      sgl += (int32_t)((hi - lo) - 4 * chunks);
-      e += (int32_t)(hi - lo);
-    }
-    R.cpre[n] = c;
-    R.spre[n] = sgl;
-    R.epre[n] = e;
-  }
-}
-
-// Rank owning flattened item k of a prefix array (largest r with pre[r] <= k).
-__device__ __forceinline__ int owner_rank(const int32_t* pre, int n, int32_t k) {
-  int lo = 0, hi = n;  // pre[lo] <= k < pre[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (pre[mid] <= k) lo = mid;
-    else hi = mid;
-  }
-  return lo;
-}
-
-// Single entries of rank r: the head [lo, 4*vlo) and the tail after the
-// chunks (or the whole range when the list cannot be read in chunks).
-__device__ __forceinline__ int64_t single_pos(const BinRanges& R, int r, int32_t j) {
-  const int64_t lo = R.lo[r];
-  const int64_t head = min(R.vlo[r] * 4, R.hi[r]) - lo;
-  const int64_t chunks = R.cpre[r + 1] - R.cpre[r];
-  return j < head ? lo + j : lo + head + 4 * chunks + (j - head);
-}
-
-// Calls f(r, i, key, prev, val) for every entry i of every rank's range of
-// the bin, with prev = the key at i-1 (or -1 at i = 0).  kVals loads the
-// values as well.
-template <bool kVals, typename F>
-__device__ __forceinline__ void for_entries(const Lists& lists, int n, const BinRanges& R, F&& f) {
-  constexpr int kUnroll = 2;
-  const int32_t chunks = R.cpre[n];
-  for (int32_t k0 = threadIdx.x; k0 < chunks; k0 += blockDim.x * kUnroll) {
-    int4 key[kUnroll];
-    float4 val[kUnroll];
-    int32_t prev[kUnroll];
-    int rr[kUnroll];
-    int64_t at[kUnroll];
+__device__ __forceinline__ BinFetch bin_fetch(const int32_t* starts, int n, int bins, int b) {
+  const int lane = threadIdx.x & 31;
+  BinFetch f;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int32_t k = k0 + u * blockDim.x;
-      if (k < chunks) {
-        const int r = owner_rank(R.cpre, n, k);
-        const int64_t c = R.vlo[r] + (k - R.cpre[r]);
-        rr[u] = r;
-        at[u] = 4 * c;
-        key[u] = __ldg(reinterpret_cast<const int4*>(lists.idx[r]) + c);
-        prev[u] = at[u] > 0 ? __ldg(lists.idx[r] + at[u] - 1) : -1;
-        if (kVals) val[u] = __ldg(reinterpret_cast<const float4*>(lists.val[r]) + c);
+  for (int h = 0; h < 2; ++h) {
+    const int r = lane + 32 * h;
+    f.lo[h] = f.hi[h] = 0;
+    if (r < n) {
+      const int32_t* row = starts + (size_t)r * (bins + 1) + b;
+      f.lo[h] = __ldcg(row);
+      f.hi[h] = __ldcg(row + 1);
+    }
+  }
+  return f;
+}
+
+// Clamps the fetched rows to the list lengths and fills R (warp-collective;
+// ends with __syncwarp).  Returns the bin's entry count.
+__device__ __forceinline__ int bin_commit(const Lists& lists, int n, const BinFetch& f,
+                                          BinRanks& R) {
+  const int lane = threadIdx.x & 31;
+  int carry = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (32 * h >= n) break;
+    const int r = lane + 32 * h;
+    int lo = 0, len = 0;
+    if (r < n) {
+      const int nnz = (int)lists.nnz[r];
+      lo = min(max(f.lo[h], 0), nnz);
+      len = min(max(f.hi[h], lo), nnz) - lo;
+    }
+    const int incl = warp_incl_scan(len);
+    if (r < n) {
+      R.lo[r] = lo;
+      R.epre[r] = carry + incl - len;
+    }
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) R.epre[n] = carry;
+  __syncwarp();
+  return carry;
+}
+
+// Walks the bin's flattened entries 32 at a time (lane l takes position
+// k0 + l), kBatch groups per batch: load(t, rank, pos) is issued for every
+// entry of a batch, then apply(rank) runs once for the batch, where rank[t]
+// is the lane's rank in group t (-1 where the lane holds no entry).  Every
+// lane keeps a cursor on its current rank and moves it forward only when
+// its position passes the rank's end, so ranks are non-decreasing in
+// (group, lane) order.  apply is called by every lane, so it may use warp
+// collectives.
+template <typename Load, typename Apply>
+__device__ __forceinline__ void for_bin_entries(const Lists& lists, int n, const BinRanks& R,
+                                                int total, int32_t* status, Load&& load,
+                                                Apply&& apply) {
+  const int lane = threadIdx.x & 31;
+  int cr = 0, cend = R.epre[1];
+  int off = R.lo[0];  // list position = off + k inside rank cr
+  int lim = (int)lists.nnz[0];
+  for (int k0 = 0; k0 < total; k0 += 32 * kBatch) {
+    int rank[kBatch];
+#pragma unroll
+    for (int t = 0; t < kBatch; ++t) {
+      const int k = k0 + 32 * t + lane;
+      rank[t] = -1;
+      if (k < total) {
+        if (k >= cend && cr < n - 1) {
+          int cstart;
+          do {
+            ++cr;
+            cstart = cend;
+            cend = R.epre[cr + 1];
+          } while (k >= cend && cr < n - 1);
+          off = R.lo[cr] - cstart;
+          lim = (int)lists.nnz[cr];
+        }
+        const int pos = off + k;
+        if ((unsigned)pos < (unsigned)lim) {
+          rank[t] = cr;
+          load(t, cr, pos);
+        } else {
+          flag(status, ZR_ERR_INTERNAL);  // cannot happen; skipped, never read
+        }
       }
     }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int32_t k = k0 + u * blockDim.x;
-      if (k < chunks) {
-        f(rr[u], at[u] + 0, key[u].x, prev[u], kVals ? val[u].x : 0.0f);
-        f(rr[u], at[u] + 1, key[u].y, key[u].x, kVals ? val[u].y : 0.0f);
-        f(rr[u], at[u] + 2, key[u].z, key[u].y, kVals ? val[u].z : 0.0f);
-        f(rr[u], at[u] + 3, key[u].w, key[u].z, kVals ? val[u].w : 0.0f);
-      }
-    }
-  }
-  const int32_t singles = R.spre[n];
-  for (int32_t k = threadIdx.x; k < singles; k += blockDim.x) {
-    const int r = owner_rank(R.spre, n, k);
-    const int64_t i = single_pos(R, r, k - R.spre[r]);
-    const int32_t key = __ldg(lists.idx[r] + i);
-    const int32_t prev = i > 0 ? __ldg(lists.idx[r] + i - 1) : -1;
-    f(r, i, key, prev, kVals ? __ldg(lists.val[r] + i) : 0.0f);
+    apply(k0, rank);
   }
 }
 
 // ------------------------------------------------------------ 2. count
-__global__ void __launch_bounds__(kThreads)
-union_count_kernel(const __grid_constant__ Lists lists, int n, int64_t dense_size, int log_w,
-                   int words, int64_t bins, const int32_t* coarse, H0 h, int parts,
-                   int32_t* cnt_g, unsigned long long* seg_g, unsigned long long* tot_g,
-                   int32_t* wcnt_g, int32_t* status) {
-  __shared__ uint32_t ubits[kWords];
-  __shared__ int32_t cnt[ZR_MAX_PARTS];
-  __shared__ int32_t wcnt[kWarps * ZR_MAX_PARTS];
-  __shared__ BinRanges R;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int64_t W = 1ll << log_w;
+// Per bin, a warp builds the bin's union bitmap and counts its members per
+// partition; lane p then publishes cnt[p][b].  Sparse bins (fewer entries
+// than W/4) count at the entry that sets a bit (the first holder); dense
+// bins OR every key in without waiting for the old word and then hash the
+// bitmap one word per step, a lane per key.  Bins are dealt to warps with a
+// grid-wide stride, so a dense region of the key range is spread over many
+// warps, and no warp waits on another.
+__global__ void __launch_bounds__(kBinThreads)
+bin_count_kernel(const __grid_constant__ Lists lists, int n, int log_w, int bins,
+                 const int32_t* starts, H0 h, int parts, int32_t* cnt_g, int32_t* status) {
+  __shared__ uint32_t ubits_all[kBinWarps][128];
+  __shared__ int32_t wc_all[kBinWarps][ZR_MAX_PARTS];
+  __shared__ BinRanks ranks_all[kBinWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t* ub = ubits_all[warp];
+  int32_t* wc = wc_all[warp];
+  BinRanks& R = ranks_all[warp];
   const H0 hash = h;
-  const int per_warp = words / kWarps;
-  for (int64_t b = blockIdx.x; b < bins; b += gridDim.x) {
-    for (int w = tid; w < words; w += kThreads) ubits[w] = 0;
-    for (int i = tid; i < kWarps * parts; i += kThreads) wcnt[i] = 0;
-    const int64_t base = b << log_w;
-    bin_ranges_load(lists, n, coarse, bins, b, R);
-    __syncthreads();
-    bin_ranges_finish(lists, n, R);
-    __syncthreads();
-    // Union bitmap; every list is checked strictly ascending and in range
-    // (the ranges of consecutive bins overlap, so every adjacent pair of
-    // every list is seen by some bin).
-    bool bad = false;
-    for_entries<false>(lists, n, R, [&](int, int64_t i, int32_t key, int32_t prev, float) {
-      if (key < 0 || key >= dense_size || (i > 0 && key <= prev)) bad = true;
-      const int64_t slot = (int64_t)key - base;
-      if (slot >= 0 && slot < W) atomicOr(&ubits[slot >> 5], 1u << (slot & 31));
-    });
-    if (bad) flag(status, ZR_ERR_INPUT_UNSORTED);
-    __syncthreads();
-    // Members per (warp, partition) over the warp's words (the same split of
-    // words the writer uses); a lane takes one half of a word at a time.
-    {
-      const int lane = tid & 31;
-      for (int hw = lane; hw < 2 * per_warp; hw += 32) {
-        const int wd = warp * per_warp + (hw >> 1);
-        uint32_t bits = ubits[wd] & ((hw & 1) ? 0xFFFF0000u : 0x0000FFFFu);
-        while (bits) {
-          const int bit = __ffs(bits) - 1;
-          bits &= bits - 1;
-          const uint32_t key = (uint32_t)(base + wd * 32 + bit);
-          atomicAdd(&wcnt[warp * parts + (parts > 1 ? (int)hash(key) : 0)], 1);
+  const int words = 1 << (log_w - 5);
+  const int W = 1 << log_w;
+  const int nwarps = gridDim.x * kBinWarps;
+  for (int p = lane; p < parts; p += 32) wc[p] = 0;
+  int b = blockIdx.x * kBinWarps + warp;
+  BinFetch fetch = {};
+  if (b < bins) fetch = bin_fetch(starts, n, bins, b);
+  for (; b < bins; b += nwarps) {
+    const uint32_t base = (uint32_t)b << log_w;
+    for (int w = lane; w < words; w += 32) ub[w] = 0;
+    const int total = bin_commit(lists, n, fetch, R);
+    if (b + nwarps < bins) fetch = bin_fetch(starts, n, bins, b + nwarps);
+    int key[kBatch];
+    auto load = [&](int t, int r, int pos) { key[t] = __ldg(lists.idx[r] + pos); };
+    if (total * 4 < W) {
+      for_bin_entries(lists, n, R, total, status, load, [&](int, const int (&rank)[kBatch]) {
+#pragma unroll
+        for (int t = 0; t < kBatch; ++t) {
+          const uint32_t slot = (uint32_t)key[t] - base;
+          if (rank[t] >= 0 && slot < (uint32_t)W) {
+            const uint32_t bit = 1u << (slot & 31);
+            if (!(atomicOr(&ub[slot >> 5], bit) & bit)) {
+              const int p = parts > 1 ? (int)hash((uint32_t)key[t]) : 0;
+              if ((unsigned)p < (unsigned)parts) atomicAdd(&wc[p], 1);
+              else flag(status, ZR_ERR_INTERNAL);
+            }
+          }
+        }
+      });
+      __syncwarp();
+    } else {
+      for_bin_entries(lists, n, R, total, status, load, [&](int, const int (&rank)[kBatch]) {
+#pragma unroll
+        for (int t = 0; t < kBatch; ++t) {
+          const uint32_t slot = (uint32_t)key[t] - base;
+          if (rank[t] >= 0 && slot < (uint32_t)W) atomicOr(&ub[slot >> 5], 1u << (slot & 31));
+        }
+      });
+      __syncwarp();
+      for (int w = 0; w < words; ++w) {
+        if ((ub[w] >> lane) & 1u) {
+          const int p = parts > 1 ? (int)hash(base + (uint32_t)(w * 32 + lane)) : 0;
+          if ((unsigned)p < (unsigned)parts) atomicAdd(&wc[p], 1);
+          else flag(status, ZR_ERR_INTERNAL);
         }
       }
+      __syncwarp();
     }
-    __syncthreads();
-    for (int p = tid; p < parts; p += kThreads) {
-      int s = 0;
-      for (int w = 0; w < kWarps; ++w) s += wcnt[w * parts + p];
-      cnt[p] = s;
+    for (int p = lane; p < parts; p += 32) {
+      __stcg(cnt_g + (size_t)p * bins + b, wc[p]);
+      wc[p] = 0;
     }
-    if (wcnt_g)
-      for (int i = tid; i < kWarps * parts; i += kThreads) __stcg(wcnt_g + b * kWarps * parts + i, wcnt[i]);
-    __syncthreads();
-    publish_counts(b, cnt, parts, cnt_g, seg_g, tot_g);
-    __syncthreads();
+    __syncwarp();
   }
 }
 
-// ------------------------------------------------------------ 3. write
-// Shared memory of the writer: the bin's window of folded values, its union
-// bitmap, its staged entries (rank-major) and the per-warp output bases.
-__host__ __device__ inline size_t write_smem_bytes(int parts) {
-  return (size_t)kWords * 32 * 4 + (size_t)kWords * 4 + (size_t)kStage * 8 +
-         (size_t)kWarps * parts * 8 + (size_t)parts * 8;
+// ------------------------------------------------------------ 3. scan
+// Two launches over grid (chunk of 2048 bins, partition): the first sums
+// each chunk's counts, the second adds the earlier chunks' sums (the carry)
+// to a block-wide scan of its chunk: excl[p][b] = sum_{b' < b} cnt[p][b'].
+// The last chunk also writes the partition total.
+__device__ __forceinline__ long long block_sum(long long v, long long* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  long long t = 0;
+  if (warp == 0) {
+    t = lane < (int)(blockDim.x >> 5) ? red[lane] : 0;
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  }
+  return t;  // valid in warp 0
 }
 
-__global__ void __launch_bounds__(kThreads)
-union_write_kernel(const __grid_constant__ Lists lists, int n, int64_t bins, const int32_t* coarse,
-                   H0 h, int parts, int average, const int32_t* cnt_g,
-                   const unsigned long long* seg_g, const unsigned long long* tot_g,
-                   const int32_t* wcnt_g, int32_t* out_idx, float* out_val, int64_t out_cap,
-                   int64_t* d_offsets, int64_t* d_total, int32_t* status) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ BinRanges R;
-  __shared__ long long offs[ZR_MAX_PARTS + 1];
-  float* acc = reinterpret_cast<float*>(smem);                       // [W]
-  uint32_t* ubits = reinterpret_cast<uint32_t*>(acc + kWords * 32);  // [words]
-  int32_t* skey = reinterpret_cast<int32_t*>(ubits + kWords);        // [kStage]
-  float* sval = reinterpret_cast<float*>(skey + kStage);             // [kStage]
-  long long* wbase = reinterpret_cast<long long*>(sval + kStage);    // [kWarps][parts]
-  long long* ubase = wbase + kWarps * parts;                         // [parts]
-  const int tid = threadIdx.x, warp = tid >> 5;
-  constexpr int W = 1 << kLogW;
-  constexpr int per_warp = kWords / kWarps;
-  const float fn = (float)n;
-  const H0 hash = h;
-  partition_offsets(tot_g, parts, offs, d_offsets, d_total);
+__global__ void __launch_bounds__(kScanThreads)
+bin_chunk_sum_kernel(const int32_t* cnt_g, int bins, long long* ctot_g) {
+  __shared__ long long red[kScanThreads / 32];
+  const int c = blockIdx.x, p = blockIdx.y, chunks = gridDim.x;
+  const int b0 = (c << kChunkLog) + threadIdx.x * 2;
+  const int32_t* row = cnt_g + (size_t)p * bins;
+  long long v = 0;
+  if (b0 < bins) v += __ldcg(row + b0);
+  if (b0 + 1 < bins) v += __ldcg(row + b0 + 1);
+  const long long t = block_sum(v, red);
+  if (threadIdx.x == 0) ctot_g[(size_t)p * chunks + c] = t;
+}
 
-  for (int64_t b = blockIdx.x; b < bins; b += gridDim.x) {
-    const int64_t base = b << kLogW;
-    // Every global load of the prologue is issued before one barrier: the
-    // sampled bounds, the position sums and the per-warp member counts.
-    for (int i = tid; i < W; i += kThreads) acc[i] = -0.0f;
-    for (int i = tid; i < kWords; i += kThreads) ubits[i] = 0;
-    bin_ranges_load(lists, n, coarse, bins, b, R);
-    unit_base(b, parts, offs, cnt_g, seg_g, ubase);
-    for (int i = tid; i < kWarps * parts; i += kThreads)
-      wbase[i] = wcnt_g ? (long long)__ldcg(wcnt_g + b * kWarps * parts + i) : 0;
-    __syncthreads();
-    bin_ranges_finish(lists, n, R);
-    for (int p = tid; p < parts; p += kThreads) {  // per-warp bases
-      long long run = ubase[p];
-      for (int w = 0; w < kWarps; ++w) {
-        const long long c = wbase[w * parts + p];
-        wbase[w * parts + p] = run;
-        if (wcnt_g) run += c;
-      }
+__global__ void __launch_bounds__(kScanThreads)
+bin_scan_kernel(const int32_t* cnt_g, const long long* ctot_g, int bins, long long* excl_g,
+                long long* tot_g) {
+  __shared__ long long red[kScanThreads / 32];
+  __shared__ long long s_carry;
+  const int c = blockIdx.x, p = blockIdx.y, chunks = gridDim.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  long long before = 0;
+  for (int j = tid; j < c; j += kScanThreads) before += __ldcg(ctot_g + (size_t)p * chunks + j);
+  const long long carry_sum = block_sum(before, red);
+  if (tid == 0) s_carry = carry_sum;
+  __syncthreads();
+  const int b0 = (c << kChunkLog) + tid * 2;
+  const int32_t* row = cnt_g + (size_t)p * bins;
+  const int v0 = b0 < bins ? __ldcg(row + b0) : 0;
+  const int v1 = b0 + 1 < bins ? __ldcg(row + b0 + 1) : 0;
+  const int s = v0 + v1;
+  const int incl = warp_incl_scan(s);
+  if (lane == 31) red[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const long long x = red[lane];
+    long long xi = x;
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, xi, o);
+      if (lane >= o) xi += y;
     }
-    __syncthreads();
-    const int total = R.epre[n];
-    if (total <= kStage) {
-      // Stage every rank's range at once (16-byte loads, many in flight).
-      for_entries<true>(lists, n, R, [&](int r, int64_t i, int32_t key, int32_t, float v) {
-        const int e = R.epre[r] + (int)(i - R.lo[r]);
-        skey[e] = key;
-        sval[e] = v;
-      });
-      __syncthreads();
-      // Fold rank by rank in ascending rank order: acc starts at -0.0 and
-      // -0.0 + x == x, so each member ends as the left fold of its holders.
-      for (int r = 0; r < n; ++r) {
-        for (int e = R.epre[r] + tid; e < R.epre[r + 1]; e += kThreads) {
-          const int64_t slot = (int64_t)skey[e] - base;
-          if (slot >= 0 && slot < W) {
-            acc[slot] = __fadd_rn(acc[slot], sval[e]);
-            atomicOr(&ubits[slot >> 5], 1u << (slot & 31));
-          }
-        }
-        __syncthreads();
-      }
-    } else {
-      // A bin too large to stage: the same fold straight from the lists.
-      __syncthreads();
-      for (int r = 0; r < n; ++r) {
-        const int32_t* idx = lists.idx[r];
-        const float* val = lists.val[r];
-        for (int64_t i = R.lo[r] + tid; i < R.hi[r]; i += kThreads) {
-          const int64_t slot = (int64_t)idx[i] - base;
-          if (slot >= 0 && slot < W) {
-            acc[slot] = __fadd_rn(acc[slot], val[i]);
-            atomicOr(&ubits[slot >> 5], 1u << (slot & 31));
-          }
-        }
-        __syncthreads();
-      }
+    red[lane] = xi - x;
+    if (lane == 31 && c == chunks - 1) tot_g[p] = s_carry + xi;
+  }
+  __syncthreads();
+  const long long run = s_carry + red[warp] + (incl - s);
+  long long* out = excl_g + (size_t)p * bins;
+  if (b0 < bins) out[b0] = run;
+  if (b0 + 1 < bins) out[b0 + 1] = run + v0;
+}
+
+// ------------------------------------------------------------ 4. write
+// offs[0..parts] = exclusive prefix of the partition totals (shared memory);
+// block 0 of the grid also writes d_offsets and the grand total.
+__device__ void load_partition_offsets(const long long* tot_g, int parts, long long* offs,
+                                       int64_t* d_offsets, int64_t* d_total) {
+  for (int p = threadIdx.x; p < parts; p += blockDim.x) offs[p] = __ldcg(tot_g + p);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long acc = 0;
+    for (int p = 0; p < parts; ++p) {
+      const long long t = offs[p];
+      offs[p] = acc;
+      acc += t;
     }
-    const int c0 = warp * per_warp, c1 = c0 + per_warp;
-    if (!wcnt_g) {
-      // Count members per (warp, partition), then an exclusive scan over warps.
-      for_members(ubits, c0, c1, base, hash, parts,
-                  [&](bool live, uint32_t, int, int, int p, unsigned peers) {
-                    if (live && (peers & lanemask_lt()) == 0) wbase[warp * parts + p] += __popc(peers);
-                    __syncwarp();
-                  });
-      __syncthreads();
-      for (int p = tid; p < parts; p += kThreads) {
-        long long run = ubase[p];
-        for (int w = 0; w < kWarps; ++w) {
-          const long long t = wbase[w * parts + p] - ubase[p];
-          wbase[w * parts + p] = run;
-          run += t;
-        }
-      }
-      __syncthreads();
+    offs[parts] = acc;
+    if (blockIdx.x == 0) {
+      if (d_offsets)
+        for (int p = 0; p <= parts; ++p) d_offsets[p] = offs[p];
+      if (d_total) *d_total = acc;
     }
-    // Place and write the members in ascending key order per partition.
-    for_members(ubits, c0, c1, base, hash, parts,
-                [&](bool live, uint32_t key, int wd, int bit, int p, unsigned peers) {
-                  if (live) {
-                    const long long dst = wbase[warp * parts + p] + __popc(peers & lanemask_lt());
-                    float v = acc[wd * 32 + bit];
-                    if (average) v = __fdiv_rn(v, fn);
-                    if (dst >= 0 && dst < out_cap) {
-                      out_idx[dst] = (int32_t)key;
-                      out_val[dst] = v;
-                    } else {
-                      flag(status, ZR_ERR_INPUT_UNSORTED);
-                    }
+  }
+  __syncthreads();
+}
+
+// Warp-private shared memory of the writer: acc[W] (f32, first, so that it
+// is 16-byte aligned), wdelta[parts] (i64), ub[W/32], run[parts] (i32),
+// mlist[W] and stage[W] (u16).
+__host__ __device__ inline size_t warp_smem_bytes(int log_w, int parts) {
+  const size_t W = (size_t)1 << log_w;
+  const size_t b = (size_t)parts * 8 + W * 4 + (W / 32) * 4 + (size_t)parts * 4 + W * 2 + W * 2;
+  return (b + 15) & ~(size_t)15;
+}
+
+// Per bin:
+//   fold    entries in flattened rank-major order into acc[]; inside a group
+//           of 32 the lanes are applied one rank at a time, lowest first, so
+//           every member is the left fold of its holders in rank order (the
+//           bitmap's old bit says whether a slot already holds a value);
+//   list    the members' slots in ascending key order (mlist);
+//   place   a counting sort of mlist by partition into stage[], stable, so
+//           stage[] is the bin's output in partition-major, ascending-key
+//           order (run[p] starts at the bin-local prefix of the counts);
+//   emit    stage[] 32 entries at a time; entry j of partition p goes to
+//           offs[p] + excl[p][b] + (j - pstart[p]), so each partition's run
+//           of the bin leaves as one contiguous, coalesced store.
+__global__ void __launch_bounds__(kWriteThreads)
+bin_write_kernel(const __grid_constant__ Lists lists, int n, int log_w, int bins,
+                 const int32_t* starts, H0 h, int parts, int average, const int32_t* cnt_g,
+                 const long long* excl_g, const long long* tot_g, int32_t* out_idx,
+                 float* out_val, int64_t out_cap, int64_t* d_offsets, int64_t* d_total,
+                 int32_t* status) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ long long offs[ZR_MAX_PARTS + 1];
+  __shared__ BinRanks ranks_all[kWriteWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  BinRanks& R = ranks_all[warp];
+  const int W = 1 << log_w;
+  const int words = W >> 5, wpl = words >> 5;
+  unsigned char* mine = smem + (size_t)warp * warp_smem_bytes(log_w, parts);
+  float* acc = reinterpret_cast<float*>(mine);
+  long long* wdelta = reinterpret_cast<long long*>(acc + W);
+  uint32_t* ub = reinterpret_cast<uint32_t*>(wdelta + parts);
+  int32_t* run = reinterpret_cast<int32_t*>(ub + words);
+  uint16_t* mlist = reinterpret_cast<uint16_t*>(run + parts);
+  uint16_t* stage = mlist + W;
+  const H0 hash = h;
+  const float fn = (float)n;
+  const unsigned lt = lanemask_lt();
+  load_partition_offsets(tot_g, parts, offs, d_offsets, d_total);
+
+  const int nwarps = gridDim.x * kWriteWarps;
+  int b = blockIdx.x * kWriteWarps + warp;
+  BinFetch fetch = {};
+  if (b < bins) fetch = bin_fetch(starts, n, bins, b);
+  for (; b < bins; b += nwarps) {
+    const uint32_t base = (uint32_t)b << log_w;
+    for (int w = lane; w < words; w += 32) ub[w] = 0;
+    // -0.0 is the identity of the fold: -0.0 + x == x for every x that is
+    // not a NaN, so each member ends as the left fold of its holders.
+    for (int i = lane; i < (W >> 2); i += 32)
+      reinterpret_cast<float4*>(acc)[i] = make_float4(-0.0f, -0.0f, -0.0f, -0.0f);
+    // This bin's partition runs: pstart[p] (bin-local) and the global base.
+    int expect = 0, run0 = 0;
+    for (int p0 = 0; p0 < parts; p0 += 32) {
+      const int p = p0 + lane;
+      const int c = p < parts ? __ldcg(cnt_g + (size_t)p * bins + b) : 0;
+      const long long e = p < parts ? __ldcg(excl_g + (size_t)p * bins + b) : 0;
+      const int incl = warp_incl_scan(c);
+      if (p0 == 0) run0 = incl - c;
+      if (p < parts) {
+        run[p] = expect + incl - c;
+        wdelta[p] = offs[p] + e - (expect + incl - c);
+      }
+      expect += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    const int total = bin_commit(lists, n, fetch, R);
+    if (b + nwarps < bins) fetch = bin_fetch(starts, n, bins, b + nwarps);
+
+    int key[kBatch];
+    float val[kBatch];
+    for_bin_entries(
+        lists, n, R, total, status,
+        [&](int t, int r, int pos) {
+          key[t] = __ldg(lists.idx[r] + pos);
+          val[t] = __ldg(lists.val[r] + pos);
+        },
+        [&](int k0, const int (&rank)[kBatch]) {
+          // Group by group.  Keys that strictly ascend across the lanes of
+          // a group are all distinct, so such a group is applied at once;
+          // otherwise each maximal ascending run of lanes is applied in
+          // lane order (ranks never decrease along the lanes, so a key held
+          // by two ranks meets the lower rank first).
+#pragma unroll
+          for (int t = 0; t < kBatch; ++t) {
+            if (k0 + 32 * t < total) {
+              const uint32_t slot = (uint32_t)key[t] - base;
+              const bool live = rank[t] >= 0;
+              const bool in = live && slot < (uint32_t)W;
+              const int prev = __shfl_up_sync(0xffffffffu, key[t], 1);
+              const unsigned desc = __ballot_sync(0xffffffffu, live && lane > 0 && prev >= key[t]);
+              if (desc == 0) {
+                if (in) {
+                  acc[slot] = __fadd_rn(acc[slot], val[t]);
+                  atomicOr(&ub[slot >> 5], 1u << (slot & 31));
+                }
+              } else {
+                const int run_id = __popc(desc & (lt | (1u << lane)));
+                const int runs = __popc(desc) + 1;
+                for (int q = 0; q < runs; ++q) {
+                  if (in && run_id == q) {
+                    acc[slot] = __fadd_rn(acc[slot], val[t]);
+                    atomicOr(&ub[slot >> 5], 1u << (slot & 31));
                   }
                   __syncwarp();
-                  if (live && (peers & lanemask_lt()) == 0) wbase[warp * parts + p] += __popc(peers);
-                  __syncwarp();
-                });
-    __syncthreads();
+                }
+              }
+              __syncwarp();
+            }
+          }
+        });
+    __syncwarp();
+
+    // list: lane l owns words [l * wpl, (l + 1) * wpl)
+    int mine_cnt = 0;
+    for (int q = 0; q < wpl; ++q) mine_cnt += __popc(ub[lane * wpl + q]);
+    const int incl = warp_incl_scan(mine_cnt);
+    const int members = __shfl_sync(0xffffffffu, incl, 31);
+    if (members != expect) {
+      // The count pass saw the same entries, so this cannot happen.
+      if (lane == 0) flag(status, ZR_ERR_INTERNAL);
+      __syncwarp();
+      continue;
+    }
+    int at = incl - mine_cnt;
+    for (int q = 0; q < wpl; ++q) {
+      const int w = lane * wpl + q;
+      uint32_t bits = ub[w];
+      while (bits) {
+        const int bit = __ffs(bits) - 1;
+        bits &= bits - 1;
+        mlist[at++] = (uint16_t)(w * 32 + bit);
+      }
+    }
+    __syncwarp();
+
+    // place
+    if (parts <= 32) {
+      // Lane q keeps partition q's next stage position.  Per step of 32
+      // members, nbits ballots of the partition bits give every lane the
+      // set of lanes that share its partition (its rank among them) and
+      // lane q the number of members in partition q.
+      const int nbits = parts > 1 ? 32 - __clz(parts - 1) : 0;
+      int runq = run0;
+      for (int j0 = 0; j0 < members; j0 += 32) {
+        const int j = j0 + lane;
+        bool live = j < members;
+        const int slot = live ? mlist[j] : 0;
+        int p = parts > 1 ? (int)hash(base + (uint32_t)slot) : 0;
+        if (live && (unsigned)p >= (unsigned)parts) {
+          flag(status, ZR_ERR_INTERNAL);
+          live = false;
+        }
+        if (!live) p = 0;
+        const unsigned all = __ballot_sync(0xffffffffu, live);
+        unsigned same = all, mine_q = all;
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {
+          if (i < nbits) {
+            const unsigned bi = __ballot_sync(0xffffffffu, (p >> i) & 1);
+            same &= ((p >> i) & 1) ? bi : ~bi;
+            mine_q &= ((lane >> i) & 1) ? bi : ~bi;
+          }
+        }
+        const int at_p = __shfl_sync(0xffffffffu, runq, p);
+        if (live) {
+          const int sidx = at_p + __popc(same & lt);
+          if ((unsigned)sidx < (unsigned)members) stage[sidx] = (uint16_t)slot;
+          else flag(status, ZR_ERR_INTERNAL);
+        }
+        runq += __popc(mine_q);
+      }
+    } else {
+      for (int j0 = 0; j0 < members; j0 += 32) {
+        const int j = j0 + lane;
+        const bool live = j < members;
+        const int slot = live ? mlist[j] : 0;
+        int p = live ? (int)hash(base + (uint32_t)slot) : parts;
+        if (live && (unsigned)p >= (unsigned)parts) {
+          flag(status, ZR_ERR_INTERNAL);
+          p = parts;
+        }
+        const bool ok = live && p < parts;
+        const unsigned peers = __match_any_sync(0xffffffffu, p);
+        if (ok) {
+          const int sidx = run[p] + __popc(peers & lt);
+          if ((unsigned)sidx < (unsigned)members) stage[sidx] = (uint16_t)slot;
+          else flag(status, ZR_ERR_INTERNAL);
+        }
+        __syncwarp();
+        if (ok && (peers & lt) == 0) run[p] += __popc(peers);
+        __syncwarp();
+      }
+    }
+    __syncwarp();
+
+    // emit
+    for (int j = lane; j < members; j += 32) {
+      const int slot = stage[j];
+      const uint32_t k = base + (uint32_t)slot;
+      const int p = parts > 1 ? (int)hash(k) : 0;
+      if (slot < W && (unsigned)p < (unsigned)parts) {
+        const long long dst = wdelta[p] + j;
+        float v = acc[slot];
+        if (average) v = __fdiv_rn(v, fn);
+        if (dst >= 0 && dst < out_cap) {
+          out_idx[dst] = (int32_t)k;
+          out_val[dst] = v;
+        } else {
+          flag(status, ZR_ERR_INPUT_UNSORTED);
+        }
+      } else {
+        flag(status, ZR_ERR_INTERNAL);
+      }
+    }
+    __syncwarp();
   }
 }
 
@@ -699,8 +842,8 @@ int64_t grid_for(int64_t units, int blocks_per_sm) {
   return g < 1 ? 1 : g;
 }
 
-// Per-device cached occupancy (and the dynamic shared-memory opt-in of the
-// write kernels, done once per device).
+// Per-device cached occupancy, and the dynamic shared-memory opt-in of the
+// write kernels (done once per device).
 struct DeviceInfo {
   int ready = 0;
   int count_per_sm = 1;
@@ -713,10 +856,11 @@ DeviceInfo* device_info() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   DeviceInfo& d = info[dev];
   if (!d.ready) {
-    if (cudaFuncSetAttribute(union_write_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)write_smem_bytes(ZR_MAX_PARTS)) != cudaSuccess)
+    const int write_max = (int)(kWriteWarps * warp_smem_bytes(12, ZR_MAX_PARTS));
+    if (cudaFuncSetAttribute(bin_write_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             write_max) != cudaSuccess)
       return nullptr;
-    d.count_per_sm = per_sm((const void*)union_count_kernel, kThreads, 0);
+    d.count_per_sm = per_sm((const void*)bin_count_kernel, kBinThreads, 0);
     d.part_count_per_sm = per_sm((const void*)part_count_kernel, kPartThreads, 0);
     d.ready = 1;
   }
@@ -726,58 +870,69 @@ DeviceInfo* device_info() {
 }  // namespace
 
 size_t sparse_workspace_bytes(int n, int64_t dense_size, int n_parts) {
-  const Geometry g = geometry(n, dense_size);
-  return sparse_layout(n, g.bins, n_parts > 0 ? n_parts : 1).total;
+  const int parts = n_parts > 0 ? n_parts : 1;
+  const Geometry g = geometry(n, dense_size, parts, -1);  // narrowest bins: an upper bound
+  return sparse_layout(n, g.bins, parts).total;
 }
 
 zr_status sparse_launch(const int32_t* const* idx, const float* const* val, const int64_t* nnz,
                         int n, int64_t dense_size, int n_parts, uint64_t part_seed, int average,
                         int32_t* out_idx, float* out_val, int64_t out_cap, int64_t* d_out_nnz,
                         int64_t* d_offsets, void* ws, cudaStream_t stream) {
-  const Geometry g = geometry(n, dense_size);
   const int parts = n_parts > 0 ? n_parts : 1;
-  const SparseLayout L = sparse_layout(n, g.bins, parts);
-  unsigned char* w = static_cast<unsigned char*>(ws);
-  int32_t* status = reinterpret_cast<int32_t*>(w);
-  unsigned long long* tot = reinterpret_cast<unsigned long long*>(w + L.tot);
-  unsigned long long* seg = reinterpret_cast<unsigned long long*>(w + L.seg);
-  int32_t* coarse = reinterpret_cast<int32_t*>(w + L.coarse);
-  int32_t* cnt = reinterpret_cast<int32_t*>(w + L.cnt);
-  int32_t* wcnt = keep_warp_counts(g.bins, parts) ? reinterpret_cast<int32_t*>(w + L.wcnt) : nullptr;
-
   Lists lists;
-  int64_t max_nnz = 0;
+  int64_t max_nnz = 0, total_nnz = 0;
   for (int r = 0; r < ZR_MAX_RANKS; ++r) {
     const bool live = r < n && nnz[r] > 0;
     lists.idx[r] = live ? idx[r] : nullptr;
     lists.val[r] = live ? val[r] : nullptr;
     lists.nnz[r] = r < n ? nnz[r] : 0;
-    if (r < n && nnz[r] > max_nnz) max_nnz = nnz[r];
+    if (r < n) {
+      max_nnz = nnz[r] > max_nnz ? nnz[r] : max_nnz;
+      total_nnz += nnz[r];
+    }
   }
+  const Geometry g = geometry(n, dense_size, parts, total_nnz);
+  const SparseLayout L = sparse_layout(n, g.bins, parts);
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(w);
+  int32_t* starts = reinterpret_cast<int32_t*>(w + L.starts);
+  int32_t* cnt = reinterpret_cast<int32_t*>(w + L.cnt);
+  long long* excl = reinterpret_cast<long long*>(w + L.excl);
+  long long* tot = reinterpret_cast<long long*>(w + L.tot);
+  const int bins = (int)g.bins;
   const H0 h = make_h0(part_seed, (uint32_t)parts);
   DeviceInfo* dinfo = device_info();
   if (!dinfo) return ZR_ERR_CUDA;
-  // status, partition totals and segment totals start at zero
-  if (cudaMemsetAsync(w, 0, L.coarse, stream) != cudaSuccess) return ZR_ERR_CUDA;
+  // the status word starts at zero
+  if (cudaMemsetAsync(w, 0, L.starts, stream) != cudaSuccess) return ZR_ERR_CUDA;
   {
-    const int64_t samples = (max_nnz + kSample - 1) / kSample;
-    int64_t gx = (samples + 1 + 255) / 256;
+    const int64_t groups = max_nnz / 4 + 1;
+    int64_t gx = (groups + 255) / 256;
     const int64_t cap = (int64_t)sm_count() * 8;
     if (gx > cap) gx = cap;
     if (gx < 1) gx = 1;
-    sample_kernel<<<dim3((unsigned)gx, (unsigned)n), 256, 0, stream>>>(lists, dense_size, g.log_w,
-                                                                       g.bins, coarse, status);
+    bin_starts_kernel<<<dim3((unsigned)gx, (unsigned)n), 256, 0, stream>>>(
+        lists, (int)dense_size, g.log_w, bins, starts, status);
   }
-  union_count_kernel<<<(unsigned)grid_for(g.bins, dinfo->count_per_sm), kThreads, 0, stream>>>(
-      lists, n, dense_size, g.log_w, g.words, g.bins, coarse, h, parts, cnt, seg, tot, wcnt,
-      status);
+  const int chunks = (bins + kChunkBins - 1) >> kChunkLog;
+  long long* ctot = reinterpret_cast<long long*>(w + L.ctot);
   {
-    const size_t smem = write_smem_bytes(parts);
-    const int o = per_sm((const void*)union_write_kernel, kThreads, smem);
-    union_write_kernel<<<(unsigned)grid_for(g.bins, o), kThreads, smem, stream>>>(
-        lists, n, g.bins, coarse, h, parts, average, cnt, seg, tot, wcnt, out_idx, out_val,
-        out_cap, n_parts > 0 ? d_offsets : nullptr, d_out_nnz, status);
+    const int64_t warp_units = (g.bins + kBinWarps - 1) / kBinWarps;
+    bin_count_kernel<<<(unsigned)grid_for(warp_units, dinfo->count_per_sm), kBinThreads, 0,
+                       stream>>>(lists, n, g.log_w, bins, starts, h, parts, cnt, status);
   }
+  bin_chunk_sum_kernel<<<dim3((unsigned)chunks, (unsigned)parts), kScanThreads, 0, stream>>>(
+      cnt, bins, ctot);
+  bin_scan_kernel<<<dim3((unsigned)chunks, (unsigned)parts), kScanThreads, 0, stream>>>(
+      cnt, ctot, bins, excl, tot);
+  int64_t* offsets_out = n_parts > 0 ? d_offsets : nullptr;
+  const size_t smem = kWriteWarps * warp_smem_bytes(g.log_w, parts);
+  const int o = per_sm((const void*)bin_write_kernel, kWriteThreads, smem);
+  const int64_t write_units = (g.bins + kWriteWarps - 1) / kWriteWarps;
+  bin_write_kernel<<<(unsigned)grid_for(write_units, o), kWriteThreads, smem, stream>>>(
+      lists, n, g.log_w, bins, starts, h, parts, average, cnt, excl, tot, out_idx, out_val,
+      out_cap, offsets_out, d_out_nnz, status);
   return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
 }
 

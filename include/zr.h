@@ -46,7 +46,9 @@ typedef enum zr_status {
   ZR_ERR_INPUT_UNSORTED = 5, /* device-detected: sparse indices not strictly
                                 ascending or outside [0, dense_size) */
   ZR_ERR_TIMEOUT = 6,        /* device-detected: a bounded wait gave up */
-  ZR_ERR_CUDA = 7            /* a CUDA runtime call or launch failed */
+  ZR_ERR_CUDA = 7,           /* a CUDA runtime call or launch failed */
+  ZR_ERR_INTERNAL = 8        /* device-detected: an internal consistency check
+                                failed (the access was skipped) */
 } zr_status;
 
 typedef enum zr_dtype {

@@ -53,7 +53,7 @@ def test_binding_has_no_cpu_path():
 
 def test_status_strings_and_version(zr):
     assert zr.status_string(zr.ZR_OK) == "ok"
-    for code in range(8):
+    for code in range(9):
         assert zr.status_string(code)
     assert "sm_103a" in zr.version()
 
