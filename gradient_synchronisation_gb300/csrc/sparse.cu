@@ -46,6 +46,7 @@ namespace {
 constexpr int kBinWarps = 8;             // warps per CTA in the count and write kernels
 constexpr int kBinThreads = kBinWarps * 32;
 constexpr int kBatch = 8;                // entries per lane per load batch
+constexpr int kStartsUnroll = 4;         // starts kernel: groups of 4 keys per thread per step
 constexpr int kWriteWarps = 4;           // warps per CTA in the write kernel
 constexpr int kWriteThreads = kWriteWarps * 32;
 constexpr int kPartTile = 4096;          // zr_partition: entries per tile
@@ -202,37 +203,75 @@ bin_starts_kernel(const __grid_constant__ Lists lists, int dense_size, int log_w
   int32_t* row = starts + (size_t)r * (bins + 1);
   const bool vec = (reinterpret_cast<uintptr_t>(idx) & 15) == 0;
   const int groups = nnz / 4 + 1;
-  for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < groups; q += gridDim.x * blockDim.x) {
-    const int i0 = q * 4;
-    int key[4] = {0, 0, 0, 0};
-    if (vec && i0 + 4 <= nnz) {
-      const int4 k4 = __ldg(reinterpret_cast<const int4*>(idx) + q);
-      key[0] = k4.x; key[1] = k4.y; key[2] = k4.z; key[3] = k4.w;
-    } else {
+  // Each thread takes kStartsUnroll groups per step (their loads issued
+  // together), so that one wave of CTAs keeps enough bytes in flight.  The
+  // boundary logic has no per-lane branches: a bin change stores one row
+  // entry (predicated), and the rare runs of empty bins are filled only
+  // when some lane of the warp has one.  The loop condition is the same
+  // for the whole warp, so every lane reaches the warp votes.
+  constexpr int kU = kStartsUnroll;
+  const int stride = gridDim.x * blockDim.x;
+  const int warp_q0 = (blockIdx.x * blockDim.x + threadIdx.x) & ~31;
+  for (int step = 0; warp_q0 + step * kU * stride < groups; ++step) {
+    const int q0 = blockIdx.x * blockDim.x + threadIdx.x + step * kU * stride;
+    int4 kv[kU];
+    int prev[kU];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (i0 + e < nnz) key[e] = __ldg(idx + i0 + e);
-    }
-    int prev = i0 > 0 ? __ldg(idx + i0 - 1) : -1;
-    int b_prev = i0 > 0 ? bin_of(prev, log_w, bins) : -1;
-    bool bad = false;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = i0 + e;
-      if (i > nnz) break;
-      int b_here;
-      if (i < nnz) {
-        const int k = key[e];
-        if (k < 0 || k >= dense_size || (i > 0 && k <= prev)) bad = true;
-        b_here = bin_of(k, log_w, bins);
-        prev = k;
-      } else {
-        b_here = bins;
+    for (int u = 0; u < kU; ++u) {
+      const int q = q0 + u * stride;
+      const int i0 = q * 4;
+      kv[u] = make_int4(0, 0, 0, 0);
+      prev[u] = -1;
+      if (q < groups) {
+        if (vec && i0 + 4 <= nnz) {
+          kv[u] = __ldg(reinterpret_cast<const int4*>(idx) + q);
+        } else {
+          if (i0 < nnz) kv[u].x = __ldg(idx + i0);
+          if (i0 + 1 < nnz) kv[u].y = __ldg(idx + i0 + 1);
+          if (i0 + 2 < nnz) kv[u].z = __ldg(idx + i0 + 2);
+          if (i0 + 3 < nnz) kv[u].w = __ldg(idx + i0 + 3);
+        }
+        if (i0 > 0) prev[u] = __ldg(idx + i0 - 1);
       }
-      for (int bb = b_prev + 1; bb <= b_here; ++bb) row[bb] = i;
-      if (b_here > b_prev) b_prev = b_here;
     }
-    if (bad) flag(status, ZR_ERR_INPUT_UNSORTED);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int q = q0 + u * stride;
+      const int i0 = q * 4;
+      const bool in_range = q < groups;
+      const int key[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+      // p: the key before position i (-1 before the first), bp its bin.
+      int p = prev[u];
+      int bp = p < 0 ? -1 : min(p >> log_w, bins);
+      bool bad = false, gap = false;
+      int gap_lo[4], gap_hi[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = i0 + e;
+        const bool real = in_range && i < nnz;
+        // p >= key also rejects a negative first key (p is -1 there)
+        bad |= real && (key[e] >= dense_size || key[e] <= p);
+        // position nnz is the end marker: it starts every remaining bin;
+        // positions past it change nothing
+        int bk = bp;
+        if (real) bk = key[e] < 0 ? -1 : min(key[e] >> log_w, bins);
+        else if (in_range && i == nnz) bk = bins;
+        // a bin change at position i starts bins bp + 1 .. bk there; the
+        // first is stored here, the rest (empty bins) below
+        if (bk > bp) row[bp + 1] = i;
+        gap_lo[e] = bp + 2;
+        gap_hi[e] = bk;
+        gap |= bk > bp + 1;
+        bp = max(bp, bk);
+        if (real) p = key[e];
+      }
+      if (__any_sync(0xffffffffu, gap)) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          for (int bb = gap_lo[e]; bb <= gap_hi[e]; ++bb) row[bb] = i0 + e;
+      }
+      if (__any_sync(0xffffffffu, bad) && bad) flag(status, ZR_ERR_INPUT_UNSORTED);
+    }
   }
 }
 
@@ -907,9 +946,10 @@ zr_status sparse_launch(const int32_t* const* idx, const float* const* val, cons
   // the status word starts at zero
   if (cudaMemsetAsync(w, 0, L.starts, stream) != cudaSuccess) return ZR_ERR_CUDA;
   {
+    // one wave of CTAs over the n lists
     const int64_t groups = max_nnz / 4 + 1;
-    int64_t gx = (groups + 255) / 256;
-    const int64_t cap = (int64_t)sm_count() * 8;
+    int64_t gx = (groups + 256 * kStartsUnroll - 1) / (256 * kStartsUnroll);
+    const int64_t cap = ((int64_t)sm_count() * 8 + n - 1) / n;
     if (gx > cap) gx = cap;
     if (gx < 1) gx = 1;
     bin_starts_kernel<<<dim3((unsigned)gx, (unsigned)n), 256, 0, stream>>>(
