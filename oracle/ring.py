@@ -35,6 +35,23 @@ test run the literal ring on a sample of elements.
 
 Traffic counters record the number of elements each rank sends in each phase
 (15-642 notes, "communication cost": 2(N-1) steps of M/N each per worker).
+
+AllReduce_Dropout (SkipReduce, section 4.2, Algorithm 1 "AllReduce with
+Fine-Grained Skipping", ReduceOrSkip): at every Reduce-Scatter step the
+receiving rank draws, per element, whether to skip its local gradient; a
+skipped element forwards the received value unchanged, otherwise it forwards
+local + received.  The rank that first sends a slice is never asked, so its
+value is always in the sum.  The pages draw from cuRAND; here the draw of
+receiving rank r for element e (its index in the tensor) in iteration
+``step`` is the top 32 bits of output number e of SplitMix64 seeded with
+``dropout_stream(seed, step, r)`` (output number step*64 + r of
+SplitMix64(seed)), and the element is skipped when those bits are below the
+integer threshold T (T = ceil(p * 2**32) for skip probability p, so T = 0
+never skips and T = 2**32 always does).
+
+RS-only (15-642 notes, "ZeRO Stage 2": the AllReduce is replaced by a
+Reduce-Scatter and every GPU keeps only the partition it owns): the
+AllGather is not run, and only the holder's slice is a result.
 """
 
 import numpy as np
@@ -77,7 +94,25 @@ def skip_offset(mode, k, seed, step, n):
     return splitmix.random_offset(seed, step, n)
 
 
-def ring_allreduce(x, k=0, o=0, divisor=DIV_NONE, chunk=None, counters=None):
+def dropout_stream(seed, step, r):
+    """Seed of receiving rank r's draw stream in iteration ``step``."""
+    return splitmix.output(seed, step * 64 + r)
+
+
+def dropout_skips(seed, step, r, elems, threshold):
+    """Boolean array: does rank r skip each element index in ``elems``?
+
+    The element's draw is the top 32 bits of output number e of
+    SplitMix64(dropout_stream(seed, step, r)); it is skipped when the draw is
+    below ``threshold`` (an integer in [0, 2**32]).
+    """
+    s = dropout_stream(seed, step, r)
+    elems = np.asarray(elems, dtype=np.int64)
+    return np.array([(splitmix.output(s, int(e)) >> 32) < threshold for e in elems], dtype=bool)
+
+
+def ring_allreduce(x, k=0, o=0, divisor=DIV_NONE, chunk=None, counters=None, dropout=None,
+                   elem=None, rs_only=False):
     """Run the literal ring on ``x`` (shape (N, L)), in place, and return it.
 
     ``x[r]`` is rank r's buffer.  ``chunk`` gives each of the L elements its
@@ -85,6 +120,12 @@ def ring_allreduce(x, k=0, o=0, divisor=DIV_NONE, chunk=None, counters=None):
     steps are skipped (0 <= k <= N-1), ``o`` is the slice offset, ``divisor``
     one of DIV_N, DIV_N_MINUS_K, DIV_NONE.  If ``counters`` is a dict it
     receives 'rs_sent' and 'ag_sent': per-rank element counts.
+
+    ``dropout = (threshold, seed, step)`` turns on AllReduce_Dropout's
+    ReduceOrSkip at every receive; ``elem`` gives each of the L elements its
+    index in the tensor (default 0 .. L-1), which keys its draw.  With
+    ``rs_only`` the AllGather is not run (the holder of slice c keeps the
+    result; every other position holds what the Reduce-Scatter left there).
     """
     n = x.shape[0]
     length = x.shape[1]
@@ -107,7 +148,13 @@ def ring_allreduce(x, k=0, o=0, divisor=DIV_NONE, chunk=None, counters=None):
         for r in range(n):
             recv = (r - s - 1 + o) % n
             prev = (r - 1) % n
-            x[r, members[recv]] = x[r, members[recv]] + messages[prev]
+            summed = x[r, members[recv]] + messages[prev]
+            if dropout is not None:
+                threshold, dseed, dstep = dropout
+                ids = (np.arange(length) if elem is None else np.asarray(elem))[members[recv]]
+                skip = dropout_skips(dseed, dstep, r, ids, threshold)
+                summed = np.where(skip, messages[prev], summed)
+            x[r, members[recv]] = summed
 
     # The holder of slice c is rank (c - 1 - o) mod N; it applies the average.
     if divisor != DIV_NONE:
@@ -117,7 +164,7 @@ def ring_allreduce(x, k=0, o=0, divisor=DIV_NONE, chunk=None, counters=None):
             x[holder, members[c]] = x[holder, members[c]] / np.float32(d)
 
     # AllGather: N-1 steps of replacing copies.
-    for t in range(n - 1):
+    for t in range(0 if rs_only else n - 1):
         messages = []
         for r in range(n):
             send = (r + 1 + o - t) % n
@@ -133,13 +180,16 @@ def ring_allreduce(x, k=0, o=0, divisor=DIV_NONE, chunk=None, counters=None):
     return x
 
 
-def allreduce_f32(ranks, k=0, o=0, divisor=DIV_NONE, chunk=None, counters=None):
+def allreduce_f32(ranks, k=0, o=0, divisor=DIV_NONE, chunk=None, counters=None, dropout=None,
+                  elem=None, rs_only=False):
     """Ring all-reduce of float32 rank buffers; returns a new (N, L) array."""
     x = np.array(ranks, dtype=np.float32, copy=True)
-    return ring_allreduce(x, k=k, o=o, divisor=divisor, chunk=chunk, counters=counters)
+    return ring_allreduce(x, k=k, o=o, divisor=divisor, chunk=chunk, counters=counters,
+                          dropout=dropout, elem=elem, rs_only=rs_only)
 
 
-def allreduce_bf16(ranks_bits, k=0, o=0, divisor=DIV_NONE, chunk=None, counters=None):
+def allreduce_bf16(ranks_bits, k=0, o=0, divisor=DIV_NONE, chunk=None, counters=None,
+                   dropout=None, elem=None, rs_only=False):
     """Ring all-reduce of bf16 rank buffers (uint16 bit patterns).
 
     Inputs are widened exactly to float32, every message and partial sum stays
@@ -147,8 +197,26 @@ def allreduce_bf16(ranks_bits, k=0, o=0, divisor=DIV_NONE, chunk=None, counters=
     (N, L) uint16 bit patterns every rank ends with.
     """
     x = _bf16.widen(np.asarray(ranks_bits, dtype=np.uint16)).copy()
-    ring_allreduce(x, k=k, o=o, divisor=divisor, chunk=chunk, counters=counters)
+    ring_allreduce(x, k=k, o=o, divisor=divisor, chunk=chunk, counters=counters, dropout=dropout,
+                   elem=elem, rs_only=rs_only)
     return _bf16.round_rne(x)
+
+
+def holder_of(c, n, o=0):
+    """The rank that holds slice c, fully reduced, after the Reduce-Scatter."""
+    return (c - 1 - o) % n
+
+
+def dropout_threshold(p):
+    """Integer threshold T = ceil(p * 2**32) for a skip probability p in [0, 1]
+    (exact: p is taken as the binary fraction a Python float holds)."""
+    from fractions import Fraction
+
+    q = Fraction(p)
+    if not (0 <= q <= 1):
+        raise ValueError("p must be in [0, 1]")
+    t = q * (1 << 32)
+    return int(-(-t.numerator // t.denominator))
 
 
 def naive_allreduce(ranks, order):

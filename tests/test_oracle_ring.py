@@ -236,3 +236,107 @@ def test_chunking_ceil_rule():
     np.testing.assert_array_equal(ring.chunk_ids(10, 4), [0, 0, 0, 1, 1, 1, 2, 2, 2, 3])
     np.testing.assert_array_equal(ring.chunk_ids(2, 4), [0, 1])
     assert ring.chunk_ids(0, 4).size == 0
+
+
+# ------------------------------------------------------- AllReduce_Dropout
+def test_dropout_threshold_exact():
+    # T = ceil(p * 2^32) with p taken exactly as the binary fraction a float
+    # holds: 0.1 is 0x3FB999999999999A, so p * 2^32 = 429496729.600000...
+    assert ring.dropout_threshold(0.0) == 0
+    assert ring.dropout_threshold(0.5) == 1 << 31
+    assert ring.dropout_threshold(1.0) == 1 << 32
+    assert ring.dropout_threshold(0.1) == 429496730
+    assert ring.dropout_threshold(2.0 ** -32) == 1
+
+
+@pytest.mark.parametrize("n", [2, 3, 4, 5])
+def test_dropout_fold_order(n):
+    # SkipReduce Algorithm 1 (ReduceOrSkip): slice c starts with its first
+    # sender's value (never skipped); each next rank on the ring either adds
+    # its local value or forwards what it received unchanged.
+    m = 3 * n + 2
+    c_of = ring.chunk_ids(m, n)
+    thr, seed, step = 1 << 31, 7, 3
+    x = ring.ring_allreduce(symbolic_ranks(n, m), dropout=(thr, seed, step), divisor=ring.DIV_N)
+    for e in range(m):
+        c = int(c_of[e])
+        acc = ("g", c, e)
+        for t in range(1, n):
+            r = (c + t) % n
+            if not ring.dropout_skips(seed, step, r, [e], thr)[0]:
+                acc = ("+", ("g", r, e), acc)
+        want = ("/", acc, float(n))
+        for r in range(n):
+            assert comm_equal(x[r, e].t, want), (n, r, e)
+
+
+def test_dropout_extremes():
+    rng = np.random.default_rng(11)
+    n, m = 5, 53
+    x = rng.standard_normal((n, m)).astype(np.float32)
+    plain = ring.allreduce_f32(x, divisor=ring.DIV_N)
+    none = ring.allreduce_f32(x, divisor=ring.DIV_N, dropout=(0, 1, 2))
+    assert np.array_equal(plain.view(np.uint32), none.view(np.uint32))
+    # T = 2^32 skips every receiving rank: slice c keeps its start rank's value
+    allskip = ring.allreduce_f32(x, divisor=ring.DIV_N, dropout=(1 << 32, 1, 2))
+    c_of = ring.chunk_ids(m, n)
+    want = np.array([x[c_of[e], e] / np.float32(n) for e in range(m)], dtype=np.float32)
+    for r in range(n):
+        assert np.array_equal(allskip[r].view(np.uint32), want.view(np.uint32))
+
+
+def test_dropout_integer_inputs_equal_masked_sum():
+    # Small integers add exactly in fp32, so the result is the exact sum of
+    # the start rank's value and every non-skipped rank's value.
+    rng = np.random.default_rng(12)
+    n, m = 6, 97
+    x = rng.integers(-512, 512, size=(n, m)).astype(np.float32)
+    thr, seed, step = ring.dropout_threshold(0.3), 5, 9
+    got = ring.allreduce_f32(x, dropout=(thr, seed, step))
+    c_of = ring.chunk_ids(m, n)
+    for e in range(m):
+        c = int(c_of[e])
+        total = int(x[c, e])
+        for t in range(1, n):
+            r = (c + t) % n
+            if not ring.dropout_skips(seed, step, r, [e], thr)[0]:
+                total += int(x[r, e])
+        assert got[0, e] == total
+
+
+def test_dropout_skip_rate_matches_probability():
+    # Bernoulli(p) per (rank, element): over 8 ranks x 20000 elements the
+    # observed rate is within 5 sigma of p, for every rank and overall.
+    n, m, p = 8, 20000, 0.25
+    thr = ring.dropout_threshold(p)
+    sigma = (p * (1 - p) / m) ** 0.5
+    rates = []
+    for r in range(n):
+        rate = ring.dropout_skips(3, 4, r, np.arange(m), thr).mean()
+        assert abs(rate - p) < 5 * sigma, (r, rate)
+        rates.append(rate)
+    assert abs(np.mean(rates) - p) < 5 * sigma / n ** 0.5
+    # ranks draw from different streams: their skip patterns are not equal
+    a = ring.dropout_skips(3, 4, 0, np.arange(512), thr)
+    b = ring.dropout_skips(3, 4, 1, np.arange(512), thr)
+    assert not np.array_equal(a, b)
+
+
+# ----------------------------------------------------------------- RS-only
+@pytest.mark.parametrize("n,k,o", [(2, 0, 0), (4, 1, 2), (5, 3, 1), (8, 4, 7)])
+def test_rs_only_holder_slices_equal_full_ring(n, k, o):
+    rng = np.random.default_rng(13)
+    m = 4 * n + 3
+    x = rng.standard_normal((n, m)).astype(np.float32)
+    full = ring.allreduce_f32(x, k=k, o=o, divisor=ring.DIV_N)
+    counters = {}
+    rs = ring.allreduce_f32(x, k=k, o=o, divisor=ring.DIV_N, rs_only=True, counters=counters)
+    c_of = ring.chunk_ids(m, n)
+    for c in range(n):
+        h = ring.holder_of(c, n, o)
+        cols = np.nonzero(c_of == c)[0]
+        assert np.array_equal(rs[h, cols].view(np.uint32), full[0, cols].view(np.uint32))
+    # no AllGather traffic; the Reduce-Scatter sends N-1-k slices per rank
+    assert counters["ag_sent"] == [0] * n
+    per = ring.chunk_size(m, n)
+    assert sum(counters["rs_sent"]) <= n * (n - 1 - k) * per
