@@ -12,13 +12,14 @@ exists.)
 
 Two layers:
 
-* ``zr_ring_allreduce``, ``zr_skipreduce``, ``zr_sparse_aggregate``,
-  ``zr_partition``, ``zr_query_status`` ... -- the C entry points under their
-  own names, taking integers for pointers and streams; they return the
-  ``zr_status`` code.
-* ``ring_allreduce``, ``skipreduce``, ``sparse_aggregate``, ``partition`` --
-  the same calls taking torch CUDA tensors, raising ``ZrError`` on a non-OK
-  status.  PyTorch supplies device memory and the current stream only.
+* ``zr_ring_allreduce``, ``zr_skipreduce``, ``zr_skipreduce_buckets``,
+  ``zr_allreduce_dropout``, ``zr_sparse_aggregate``, ``zr_partition``,
+  ``zr_query_status`` ... -- the C entry points under their own names, taking
+  integers for pointers and streams; they return the ``zr_status`` code.
+* ``ring_allreduce``, ``skipreduce``, ``skipreduce_buckets``,
+  ``allreduce_dropout``, ``sparse_aggregate``, ``partition`` -- the same calls
+  taking torch CUDA tensors, raising ``ZrError`` on a non-OK status.  PyTorch
+  supplies device memory and the current stream only.
 """
 
 import ctypes
@@ -46,11 +47,14 @@ ZR_DIV_N_MINUS_K = 1
 ZR_DIV_NONE = 2
 ZR_MAX_RANKS = 64
 ZR_MAX_PARTS = 256
+ZR_SKIP_RS_ONLY = 1
+ZR_MAX_BUCKETS = 128
+ZR_MAX_BUCKET_BUFS = 2048
 
 EXPORTS = (
     "zr_ring_allreduce", "zr_skipreduce", "zr_sparse_aggregate", "zr_sparse_workspace_size",
     "zr_partition", "zr_partition_workspace_size", "zr_query_status", "zr_status_string",
-    "zr_version", "zr_partition_static",
+    "zr_version", "zr_partition_static", "zr_skipreduce_buckets", "zr_allreduce_dropout",
 )
 ZR_STATIC_SCRATCH_BYTES = 2 << 20
 
@@ -64,7 +68,12 @@ class ZrError(RuntimeError):
 class SkipCfg(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("k", ctypes.c_int32), ("seed", ctypes.c_uint64),
                 ("step", ctypes.c_uint64), ("divisor", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("flags", ctypes.c_int32)]
+
+
+class Bucket(ctypes.Structure):
+    _fields_ = [("bufs", ctypes.POINTER(ctypes.c_void_p)), ("m", ctypes.c_int64),
+                ("cfg", SkipCfg)]
 
 
 def _load():
@@ -87,6 +96,8 @@ def _load():
         "zr_status_string": (ctypes.c_char_p, [i32]),
         "zr_version": (ctypes.c_char_p, []),
         "zr_partition_static": (i32, [P, P, i64, i32, u64, P, P, P, P]),
+        "zr_skipreduce_buckets": (i32, [ctypes.POINTER(Bucket), i32, i32, i32, P]),
+        "zr_allreduce_dropout": (i32, [PP, i32, i64, i32, u64, u64, u64, i32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -120,6 +131,24 @@ def zr_ring_allreduce(bufs, n, m, dtype, average, stream):
 
 def zr_skipreduce(bufs, n, m, dtype, cfg, stream):
     return lib().zr_skipreduce(_ptrs(bufs), n, m, dtype, ctypes.byref(cfg), stream)
+
+
+def zr_skipreduce_buckets(buckets, n, dtype, stream):
+    """``buckets``: list of (list of n pointers, m, SkipCfg)."""
+    arr = (Bucket * max(1, len(buckets)))()
+    keep = []
+    for i, (bufs, m, cfg) in enumerate(buckets):
+        p = _ptrs(bufs)
+        keep.append(p)
+        arr[i].bufs = ctypes.cast(p, ctypes.POINTER(ctypes.c_void_p))
+        arr[i].m = m
+        arr[i].cfg = cfg
+    return lib().zr_skipreduce_buckets(arr, len(buckets), n, dtype, stream)
+
+
+def zr_allreduce_dropout(bufs, n, m, dtype, threshold, seed, step, average, stream):
+    return lib().zr_allreduce_dropout(_ptrs(bufs), n, m, dtype, threshold, seed, step, average,
+                                      stream)
 
 
 def zr_sparse_aggregate(idx, val, nnz, n, dense_size, n_parts, part_seed, average, out_idx,
@@ -208,11 +237,53 @@ def ring_allreduce(bufs, average=True, stream=None):
            "zr_ring_allreduce")
 
 
-def skipreduce(bufs, k, mode=ZR_SKIP_RANDOM, seed=0, step=0, divisor=ZR_DIV_N, stream=None):
-    """In-place SkipReduce all-reduce skipping ``k`` Reduce-Scatter steps."""
+def skipreduce(bufs, k, mode=ZR_SKIP_RANDOM, seed=0, step=0, divisor=ZR_DIV_N, rs_only=False,
+               stream=None):
+    """In-place SkipReduce all-reduce skipping ``k`` Reduce-Scatter steps
+    (``rs_only``: Reduce-Scatter only, each slice written to its holder)."""
     ptrs, n, m, dt = _dense_args(bufs)
-    cfg = SkipCfg(mode, k, seed, step, divisor, 0)
+    cfg = SkipCfg(mode, k, seed, step, divisor, ZR_SKIP_RS_ONLY if rs_only else 0)
     _check(zr_skipreduce(ptrs, n, m, dt, cfg, _stream(stream)), "zr_skipreduce")
+
+
+def skipreduce_buckets(buckets, stream=None):
+    """Selective SkipReduce over several buckets in one launch.
+
+    ``buckets``: list of dicts with ``bufs`` (list of rank tensors) and the
+    ``skipreduce`` keywords ``k``, ``mode``, ``seed``, ``step``, ``divisor``,
+    ``rs_only`` (k = 0 protects a bucket).  All buckets share N and dtype.
+    """
+    args, n, dt = [], None, None
+    for b in buckets:
+        ptrs, bn, m, bdt = _dense_args(b["bufs"])
+        if n is None:
+            n, dt = bn, bdt
+        elif bn != n or bdt != dt:
+            raise ValueError("every bucket needs the same number of ranks and dtype")
+        cfg = SkipCfg(b.get("mode", ZR_SKIP_RANDOM), b.get("k", 0), b.get("seed", 0),
+                      b.get("step", 0), b.get("divisor", ZR_DIV_N),
+                      ZR_SKIP_RS_ONLY if b.get("rs_only", False) else 0)
+        args.append((ptrs, m, cfg))
+    _check(zr_skipreduce_buckets(args, n, dt, _stream(stream)), "zr_skipreduce_buckets")
+
+
+def dropout_threshold(p):
+    """Integer threshold T = ceil(p * 2^32) for skip probability p in [0, 1]."""
+    from fractions import Fraction
+
+    q = Fraction(p)
+    if not (0 <= q <= 1):
+        raise ValueError("p must be in [0, 1]")
+    t = q * (1 << 32)
+    return -(-t.numerator // t.denominator)
+
+
+def allreduce_dropout(bufs, p, seed=0, step=0, average=True, stream=None):
+    """In-place AllReduce_Dropout: each receiving rank skips its local element
+    with probability ``p`` (SkipReduce's ReduceOrSkip)."""
+    ptrs, n, m, dt = _dense_args(bufs)
+    _check(zr_allreduce_dropout(ptrs, n, m, dt, dropout_threshold(p), seed, step,
+                                1 if average else 0, _stream(stream)), "zr_allreduce_dropout")
 
 
 def skip_fraction_to_k(p, n):

@@ -51,6 +51,16 @@ zr_status check_dense(void* const* bufs, int32_t n, int64_t m, zr_dtype dt) {
   return ZR_OK;
 }
 
+zr_status check_cfg(const zr_skip_cfg* cfg, int32_t n) {
+  if (!cfg) return ZR_ERR_INVALID_ARG;
+  if (cfg->mode != ZR_SKIP_STATIC && cfg->mode != ZR_SKIP_RANDOM) return ZR_ERR_INVALID_ARG;
+  if (cfg->k < 0 || cfg->k > n - 1) return ZR_ERR_INVALID_ARG;
+  if (cfg->divisor != ZR_DIV_N && cfg->divisor != ZR_DIV_N_MINUS_K && cfg->divisor != ZR_DIV_NONE)
+    return ZR_ERR_INVALID_ARG;
+  if ((cfg->flags & ~ZR_SKIP_RS_ONLY) != 0) return ZR_ERR_INVALID_ARG;
+  return ZR_OK;
+}
+
 zr_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
   if (!ws) return ZR_ERR_INVALID_ARG;
   if (!aligned16(ws)) return ZR_ERR_ALIGNMENT;
@@ -69,21 +79,59 @@ zr_status zr_ring_allreduce(void* const* bufs, int32_t n, int64_t m, zr_dtype dt
   if (average != 0 && average != 1) return ZR_ERR_INVALID_ARG;
   if (m == 0) return ZR_OK;
   return zr::ring_launch(bufs, n, m, dt, 0, ZR_SKIP_STATIC, 0, 0,
-                         average ? ZR_DIV_N : ZR_DIV_NONE, static_cast<cudaStream_t>(stream));
+                         average ? ZR_DIV_N : ZR_DIV_NONE, 0, 0, 0, 0,
+                         static_cast<cudaStream_t>(stream));
 }
 
 zr_status zr_skipreduce(void* const* bufs, int32_t n, int64_t m, zr_dtype dt,
                         const zr_skip_cfg* cfg, void* stream) {
   zr_status st = zr::check_dense(bufs, n, m, dt);
   if (st != ZR_OK) return st;
-  if (!cfg) return ZR_ERR_INVALID_ARG;
-  if (cfg->mode != ZR_SKIP_STATIC && cfg->mode != ZR_SKIP_RANDOM) return ZR_ERR_INVALID_ARG;
-  if (cfg->k < 0 || cfg->k > n - 1) return ZR_ERR_INVALID_ARG;
-  if (cfg->divisor != ZR_DIV_N && cfg->divisor != ZR_DIV_N_MINUS_K && cfg->divisor != ZR_DIV_NONE)
-    return ZR_ERR_INVALID_ARG;
-  if (cfg->reserved != 0) return ZR_ERR_INVALID_ARG;
+  st = zr::check_cfg(cfg, n);
+  if (st != ZR_OK) return st;
   if (m == 0) return ZR_OK;
   return zr::ring_launch(bufs, n, m, dt, cfg->k, cfg->mode, cfg->seed, cfg->step, cfg->divisor,
+                         (cfg->flags & ZR_SKIP_RS_ONLY) ? 1 : 0, 0, 0, 0,
+                         static_cast<cudaStream_t>(stream));
+}
+
+zr_status zr_skipreduce_buckets(const zr_bucket* buckets, int32_t n_buckets, int32_t n,
+                                zr_dtype dt, void* stream) {
+  if (!buckets || n_buckets < 1 || n_buckets > ZR_MAX_BUCKETS) return ZR_ERR_INVALID_ARG;
+  if (n < 1 || n > ZR_MAX_RANKS || (int64_t)n_buckets * n > ZR_MAX_BUCKET_BUFS)
+    return ZR_ERR_INVALID_ARG;
+  // Every bucket as zr_skipreduce would check it, then no overlap between
+  // the buffers of different buckets (one launch writes them all).
+  std::vector<std::pair<uintptr_t, uintptr_t>> spans;
+  for (int b = 0; b < n_buckets; ++b) {
+    const zr_bucket& B = buckets[b];
+    zr_status st = zr::check_dense(B.bufs, n, B.m, dt);
+    if (st != ZR_OK) return st;
+    st = zr::check_cfg(&B.cfg, n);
+    if (st != ZR_OK) return st;
+    if (B.m == 0) continue;
+    const uintptr_t bytes = (uintptr_t)B.m * zr::elem_size(dt);
+    for (int r = 0; r < n; ++r) {
+      const uintptr_t a = reinterpret_cast<uintptr_t>(B.bufs[r]);
+      spans.emplace_back(a, a + bytes);
+    }
+  }
+  std::sort(spans.begin(), spans.end());
+  for (size_t i = 1; i < spans.size(); ++i)
+    if (spans[i].first < spans[i - 1].second) return ZR_ERR_INVALID_ARG;  // overlap
+  return zr::ring_buckets_launch(buckets, n_buckets, n, dt, static_cast<cudaStream_t>(stream));
+}
+
+zr_status zr_allreduce_dropout(void* const* bufs, int32_t n, int64_t m, zr_dtype dt,
+                               uint64_t threshold, uint64_t seed, uint64_t step,
+                               int32_t average, void* stream) {
+  zr_status st = zr::check_dense(bufs, n, m, dt);
+  if (st != ZR_OK) return st;
+  if (average != 0 && average != 1) return ZR_ERR_INVALID_ARG;
+  if (threshold > (1ull << 32)) return ZR_ERR_INVALID_ARG;
+  if (m == 0) return ZR_OK;
+  return zr::ring_launch(bufs, n, m, dt, 0, ZR_SKIP_STATIC, 0, 0,
+                         average ? ZR_DIV_N : ZR_DIV_NONE, 0, threshold, seed, step,
                          static_cast<cudaStream_t>(stream));
 }
 

@@ -33,18 +33,35 @@
 namespace zr {
 namespace {
 
-struct RingParams {
-  const void* bufs[ZR_MAX_RANKS];
-  int64_t m;       // elements per rank
-  int64_t chunk;   // C = ceil(m / n)
-  int32_t n;       // ranks
-  int32_t k;       // skipped Reduce-Scatter steps
-  int32_t mode;    // ZR_SKIP_STATIC / ZR_SKIP_RANDOM
+// One ring operation (a tensor, or one bucket of a multi-bucket launch).
+struct RingJob {
+  int64_t m;         // elements per rank
+  int64_t chunk;     // C = ceil(m / n)
+  int32_t n;         // ranks
+  int32_t k;         // skipped Reduce-Scatter steps
+  int32_t o;         // slice offset (Random SkipReduce), 0 <= o < n
   int32_t div_kind;  // 0: none, 1: multiply by exact power-of-two reciprocal, 2: IEEE divide
   float div;
   float inv;
-  uint64_t seed;
-  uint64_t step;
+  int32_t rs_only;   // 1: write slice c only to its holder, (c - 1 - o) mod n
+  int32_t ptr_base;  // first of this job's n rank pointers in the pointer table
+  int32_t bps;       // blocks per slice
+  int32_t pad;
+  uint64_t drop_thr;   // AllReduce_Dropout threshold T (0: off)
+  uint64_t drop_seed;
+  uint64_t drop_step;
+};
+
+struct RingParams {
+  const void* bufs[ZR_MAX_RANKS];
+  RingJob job;
+};
+
+struct BucketParams {
+  const void* bufs[ZR_MAX_BUCKET_BUFS];
+  RingJob jobs[ZR_MAX_BUCKETS];
+  int32_t block_start[ZR_MAX_BUCKETS + 1];  // prefix of n * bps over the jobs
+  int32_t n_jobs;
 };
 
 constexpr int kThreads = 128;
@@ -91,35 +108,47 @@ struct Elem<__nv_bfloat16> {
   }
 };
 
-__device__ __forceinline__ float apply_div(float x, const RingParams& P) {
-  if (P.div_kind == 1) return __fmul_rn(x, P.inv);   // exact: x * 2^-j == x / 2^j
-  if (P.div_kind == 2) return __fdiv_rn(x, P.div);
+__device__ __forceinline__ float apply_div(float x, const RingJob& J) {
+  if (J.div_kind == 1) return __fmul_rn(x, J.inv);   // exact: x * 2^-j == x / 2^j
+  if (J.div_kind == 2) return __fdiv_rn(x, J.div);
   return x;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads)
-ring_fused_kernel(const __grid_constant__ RingParams P) {
+// AllReduce_Dropout: does the receiving rank with draw stream `stream` skip
+// element e?  (High 32 bits of SplitMix64 output e of that stream < T.)
+__device__ __forceinline__ bool drop_skip(uint64_t stream, int64_t e, uint64_t thr) {
+  return (splitmix_output(stream, (uint64_t)e) >> 32) < thr;
+}
+
+struct RingShared {
+  const void* src[ZR_MAX_RANKS];  // fold order of the slice
+  void* dst[ZR_MAX_RANKS];        // rank buffers (or the holder only)
+  uint64_t stream[ZR_MAX_RANKS];  // dropout: draw stream of the t-th folded rank
+};
+
+// One block's share of slice c of job J: blocks bx = 0 .. J.bps - 1 cover
+// the slice's 16-byte vectors; block 0 also takes the scalar ends.
+template <typename T, bool kDrop>
+__device__ __forceinline__ void ring_slice(const void* const* bufs, const RingJob& J, int c, int bx,
+                                           RingShared& S) {
   using E = Elem<T>;
   constexpr int V = E::kVec;
-  __shared__ const void* s_src[ZR_MAX_RANKS];
-  __shared__ void* s_dst[ZR_MAX_RANKS];
-
-  const int n = P.n;
-  const int c = blockIdx.y;
-  const int cnt = n - P.k;
-  const int o = (P.k == 0 || P.mode == ZR_SKIP_STATIC) ? 0 : random_offset(P.seed, P.step, n);
-  const int start = ((c + P.k - o) % n + n) % n;
+  const int n = J.n;
+  const int cnt = n - J.k;
+  const int start = ((c + J.k - J.o) % n + n) % n;
+  const int holder = ((c - 1 - J.o) % n + n) % n;
+  const int nd = J.rs_only ? 1 : n;
   for (int t = threadIdx.x; t < n; t += blockDim.x) {
     int r = start + t;
     if (r >= n) r -= n;
-    s_src[t] = P.bufs[r];
-    s_dst[t] = const_cast<void*>(P.bufs[t]);
+    S.src[t] = bufs[J.ptr_base + r];
+    S.dst[t] = const_cast<void*>(bufs[J.ptr_base + (J.rs_only ? holder : t)]);
+    if (kDrop) S.stream[t] = splitmix_output(J.drop_seed, J.drop_step * 64ull + (uint64_t)r);
   }
   __syncthreads();
 
-  const int64_t lo = (int64_t)c * P.chunk;
-  const int64_t hi = min(lo + P.chunk, P.m);
+  const int64_t lo = (int64_t)c * J.chunk;
+  const int64_t hi = min(lo + J.chunk, J.m);
   if (lo >= hi) return;
   int64_t vlo = (lo + V - 1) / V;
   int64_t vhi = hi / V;
@@ -127,31 +156,34 @@ ring_fused_kernel(const __grid_constant__ RingParams P) {
 
   // Scalar ends: [lo, vlo*V) and [vhi*V, hi), each fewer than V elements
   // (or the whole short slice).
-  if (blockIdx.x == 0) {
+  if (bx == 0) {
     int64_t a0 = lo, a1 = min(vlo * V, hi);
     int64_t b0 = max(vhi * V, a1), b1 = hi;
     int64_t na = a1 - a0;
     int64_t tot = na + max((int64_t)0, b1 - b0);
     for (int64_t i = threadIdx.x; i < tot; i += blockDim.x) {
       int64_t e = (i < na) ? a0 + i : b0 + (i - na);
-      float acc = E::load1(s_src[0], e);
-      for (int t = 1; t < cnt; ++t) acc = __fadd_rn(acc, E::load1(s_src[t], e));
-      acc = apply_div(acc, P);
-      for (int r = 0; r < n; ++r) E::store1(s_dst[r], e, acc);
+      float acc = E::load1(S.src[0], e);
+      for (int t = 1; t < cnt; ++t) {
+        const float x = E::load1(S.src[t], e);
+        if (!kDrop || !drop_skip(S.stream[t], e, J.drop_thr)) acc = __fadd_rn(acc, x);
+      }
+      acc = apply_div(acc, J);
+      for (int r = 0; r < nd; ++r) E::store1(S.dst[r], e, acc);
     }
   }
 
   // Aligned vectors: each thread takes kUnroll vectors a block apart and
   // issues the loads of both (up to kUnroll x kBatch 16-byte loads) before
   // folding either, so many bytes are in flight per SM.
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x * kUnroll;
-  for (int64_t j0 = vlo + (int64_t)blockIdx.x * blockDim.x * kUnroll + threadIdx.x; j0 < vhi;
+  const int64_t stride = (int64_t)J.bps * blockDim.x * kUnroll;
+  for (int64_t j0 = vlo + (int64_t)bx * blockDim.x * kUnroll + threadIdx.x; j0 < vhi;
        j0 += stride) {
     float acc[kUnroll][V];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t j = j0 + (int64_t)u * blockDim.x;
-      if (j < vhi) E::unpack(__ldcs(static_cast<const uint4*>(s_src[0]) + j), acc[u]);
+      if (j < vhi) E::unpack(__ldcs(static_cast<const uint4*>(S.src[0]) + j), acc[u]);
     }
     for (int t = 1; t < cnt; t += kBatch) {
       uint4 w[kUnroll][kBatch];
@@ -160,17 +192,21 @@ ring_fused_kernel(const __grid_constant__ RingParams P) {
         const int64_t j = j0 + (int64_t)u * blockDim.x;
 #pragma unroll
         for (int b = 0; b < kBatch; ++b)
-          if (t + b < cnt && j < vhi) w[u][b] = __ldcs(static_cast<const uint4*>(s_src[t + b]) + j);
+          if (t + b < cnt && j < vhi) w[u][b] = __ldcs(static_cast<const uint4*>(S.src[t + b]) + j);
       }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
+        const int64_t j = j0 + (int64_t)u * blockDim.x;
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
           if (t + b < cnt) {
             float f[V];
             E::unpack(w[u][b], f);
 #pragma unroll
-            for (int q = 0; q < V; ++q) acc[u][q] = __fadd_rn(acc[u][q], f[q]);
+            for (int q = 0; q < V; ++q) {
+              if (kDrop && drop_skip(S.stream[t + b], j * V + q, J.drop_thr)) continue;
+              acc[u][q] = __fadd_rn(acc[u][q], f[q]);
+            }
           }
         }
       }
@@ -180,12 +216,38 @@ ring_fused_kernel(const __grid_constant__ RingParams P) {
       const int64_t j = j0 + (int64_t)u * blockDim.x;
       if (j < vhi) {
 #pragma unroll
-        for (int q = 0; q < V; ++q) acc[u][q] = apply_div(acc[u][q], P);
+        for (int q = 0; q < V; ++q) acc[u][q] = apply_div(acc[u][q], J);
         const uint4 out = E::pack(acc[u]);
-        for (int r = 0; r < n; ++r) __stcs(static_cast<uint4*>(s_dst[r]) + j, out);
+        for (int r = 0; r < nd; ++r) __stcs(static_cast<uint4*>(S.dst[r]) + j, out);
       }
     }
   }
+}
+
+// One job: blockIdx.y is the slice, blockIdx.x the block inside it.
+template <typename T, bool kDrop>
+__global__ void __launch_bounds__(kThreads)
+ring_fused_kernel(const __grid_constant__ RingParams P) {
+  __shared__ RingShared S;
+  ring_slice<T, kDrop>(P.bufs, P.job, blockIdx.y, blockIdx.x, S);
+}
+
+// Many jobs (buckets) in one launch: block i belongs to the job whose block
+// range holds it, then to slice (i - start) / bps of that job.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+ring_buckets_kernel(const __grid_constant__ BucketParams P) {
+  __shared__ RingShared S;
+  const int i = blockIdx.x;
+  int lo = 0, hi = P.n_jobs - 1;
+  while (lo < hi) {  // last job whose start <= i
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.block_start[mid] <= i) lo = mid;
+    else hi = mid - 1;
+  }
+  const RingJob& J = P.jobs[lo];
+  const int local = i - P.block_start[lo];
+  ring_slice<T, false>(P.bufs, J, local / J.bps, local % J.bps, S);
 }
 
 // Grid: blockIdx.y is the slice; blockIdx.x covers the slice's vectors with
@@ -194,44 +256,96 @@ ring_fused_kernel(const __grid_constant__ RingParams P) {
 // than a one-wave persistent grid (consecutive blocks sweep consecutive
 // addresses), and evict-first stores beat write-back stores by a wide margin.
 template <typename T>
-zr_status launch(const RingParams& P, cudaStream_t stream) {
+int blocks_per_slice(int64_t chunk) {
   constexpr int V = Elem<T>::kVec;
-  const int64_t vecs_per_chunk = (P.chunk + V - 1) / V;
+  const int64_t vecs_per_chunk = (chunk + V - 1) / V;
   const int64_t per_block = (int64_t)kThreads * kUnroll;
   int64_t gx = (vecs_per_chunk * 4 + per_block * 5 - 1) / (per_block * 5);
   if (gx > 0x7fffffff) gx = 0x7fffffff;
   if (gx < 1) gx = 1;
-  dim3 grid((unsigned)gx, (unsigned)P.n);
-  ring_fused_kernel<T><<<grid, kThreads, 0, stream>>>(P);
+  return (int)gx;
+}
+
+// Fills a job from validated arguments.
+RingJob make_job(int n, int64_t m, int k, int mode, uint64_t seed, uint64_t step, int divisor,
+                 int rs_only) {
+  RingJob J = {};
+  J.m = m;
+  J.chunk = (m + n - 1) / n;
+  J.n = n;
+  J.k = k;
+  J.o = (k == 0 || mode == ZR_SKIP_STATIC) ? 0 : random_offset(seed, step, n);
+  int d = divisor == ZR_DIV_N ? n : (divisor == ZR_DIV_N_MINUS_K ? n - k : 1);
+  J.div = (float)d;
+  J.inv = 1.0f;
+  if (divisor == ZR_DIV_NONE || d == 1) {
+    J.div_kind = 0;
+  } else if ((d & (d - 1)) == 0) {
+    J.div_kind = 1;
+    J.inv = 1.0f / (float)d;  // exact for a power of two
+  } else {
+    J.div_kind = 2;
+  }
+  J.rs_only = rs_only;
+  return J;
+}
+
+template <typename T>
+zr_status launch_one(RingParams& P, cudaStream_t stream) {
+  P.job.bps = blocks_per_slice<T>(P.job.chunk);
+  dim3 grid((unsigned)P.job.bps, (unsigned)P.job.n);
+  if (P.job.drop_thr != 0) ring_fused_kernel<T, true><<<grid, kThreads, 0, stream>>>(P);
+  else ring_fused_kernel<T, false><<<grid, kThreads, 0, stream>>>(P);
   return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
 }
 
 }  // namespace
 
 zr_status ring_launch(void* const* bufs, int n, int64_t m, zr_dtype dt, int k, int mode,
-                      uint64_t seed, uint64_t step, int divisor, cudaStream_t stream) {
+                      uint64_t seed, uint64_t step, int divisor, int rs_only, uint64_t drop_thr,
+                      uint64_t drop_seed, uint64_t drop_step, cudaStream_t stream) {
   RingParams P;
   for (int r = 0; r < ZR_MAX_RANKS; ++r) P.bufs[r] = r < n ? bufs[r] : nullptr;
-  P.m = m;
-  P.chunk = (m + n - 1) / n;
-  P.n = n;
-  P.k = k;
-  P.mode = mode;
-  P.seed = seed;
-  P.step = step;
-  int d = divisor == ZR_DIV_N ? n : (divisor == ZR_DIV_N_MINUS_K ? n - k : 1);
-  P.div = (float)d;
-  P.inv = 1.0f;
-  if (divisor == ZR_DIV_NONE || d == 1) {
-    P.div_kind = 0;
-  } else if ((d & (d - 1)) == 0) {
-    P.div_kind = 1;
-    P.inv = 1.0f / (float)d;  // exact for a power of two
-  } else {
-    P.div_kind = 2;
-  }
+  P.job = make_job(n, m, k, mode, seed, step, divisor, rs_only);
+  P.job.drop_thr = drop_thr;
+  P.job.drop_seed = drop_seed;
+  P.job.drop_step = drop_step;
   if (m == 0) return ZR_OK;
-  return dt == ZR_F32 ? launch<float>(P, stream) : launch<__nv_bfloat16>(P, stream);
+  return dt == ZR_F32 ? launch_one<float>(P, stream) : launch_one<__nv_bfloat16>(P, stream);
+}
+
+zr_status ring_buckets_launch(const zr_bucket* buckets, int n_buckets, int n, zr_dtype dt,
+                              cudaStream_t stream) {
+  BucketParams* P = new BucketParams();  // ~27 KB: off the host stack
+  int jobs = 0;
+  int64_t blocks = 0;
+  for (int b = 0; b < n_buckets; ++b) {
+    const zr_bucket& B = buckets[b];
+    if (B.m == 0) continue;
+    RingJob J = make_job(n, B.m, B.cfg.k, B.cfg.mode, B.cfg.seed, B.cfg.step, B.cfg.divisor,
+                         (B.cfg.flags & ZR_SKIP_RS_ONLY) ? 1 : 0);
+    J.bps = dt == ZR_F32 ? blocks_per_slice<float>(J.chunk) : blocks_per_slice<__nv_bfloat16>(J.chunk);
+    J.ptr_base = jobs * n;
+    for (int r = 0; r < n; ++r) P->bufs[jobs * n + r] = B.bufs[r];
+    P->jobs[jobs] = J;
+    P->block_start[jobs] = (int32_t)blocks;
+    blocks += (int64_t)J.bps * n;
+    ++jobs;
+  }
+  if (jobs == 0) {
+    delete P;
+    return ZR_OK;
+  }
+  if (blocks > 0x7fffffff) {
+    delete P;
+    return ZR_ERR_UNSUPPORTED;
+  }
+  P->block_start[jobs] = (int32_t)blocks;
+  P->n_jobs = jobs;
+  if (dt == ZR_F32) ring_buckets_kernel<float><<<(unsigned)blocks, kThreads, 0, stream>>>(*P);
+  else ring_buckets_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, 0, stream>>>(*P);
+  delete P;
+  return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
 }
 
 }  // namespace zr

@@ -184,9 +184,6 @@ SparseLayout sparse_layout(int n, int64_t bins, int parts) {
   return L;
 }
 
-__device__ __forceinline__ int bin_of(int key, int log_w, int bins) {
-  return key < 0 ? -1 : min(key >> log_w, bins);
-}
 
 // ------------------------------------------------------------ 1. starts
 // Grid: x over groups of 4 positions (the last group holds position nnz,

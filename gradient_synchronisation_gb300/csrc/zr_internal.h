@@ -15,7 +15,12 @@ int sm_count();
 
 // Dense ring all-reduce / SkipReduce launch; arguments already validated.
 zr_status ring_launch(void* const* bufs, int n, int64_t m, zr_dtype dt, int k, int mode,
-                      uint64_t seed, uint64_t step, int divisor, cudaStream_t stream);
+                      uint64_t seed, uint64_t step, int divisor, int rs_only, uint64_t drop_thr,
+                      uint64_t drop_seed, uint64_t drop_step, cudaStream_t stream);
+
+// Multi-bucket SkipReduce in one launch; arguments already validated.
+zr_status ring_buckets_launch(const zr_bucket* buckets, int n_buckets, int n, zr_dtype dt,
+                              cudaStream_t stream);
 
 // Sparse aggregation; arguments already validated.
 size_t sparse_workspace_bytes(int n, int64_t dense_size, int n_parts);

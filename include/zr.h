@@ -88,14 +88,22 @@ typedef enum zr_divisor {
  * mix(z) = z ^= z>>30; z *= 0xBF58476D1CE4E5B9; z ^= z>>27;
  *          z *= 0x94D049BB133111EB; z ^= z>>31.
  * With k = 0 the offset is 0 in both modes (p = 0 is exactly the plain ring).
+ *   flags    0, or ZR_SKIP_RS_ONLY: run the Reduce-Scatter only [15-642
+ *            notes, "ZeRO Stage 2": Reduce-Scatter replaces AllReduce and
+ *            each GPU keeps only its own partition].  Slice c is then written
+ *            only to its holder, rank (c - 1 - o) mod n, the rank where the
+ *            Reduce-Scatter ends; every other element of every buffer keeps
+ *            its input value.
  */
+#define ZR_SKIP_RS_ONLY 1
+
 typedef struct zr_skip_cfg {
   int32_t mode;
   int32_t k;
   uint64_t seed;
   uint64_t step;
   int32_t divisor;
-  int32_t reserved; /* must be 0 */
+  int32_t flags; /* 0 or ZR_SKIP_RS_ONLY */
 } zr_skip_cfg;
 
 /*
@@ -131,6 +139,60 @@ zr_status zr_ring_allreduce(void* const* bufs, int32_t n, int64_t m, zr_dtype dt
  */
 zr_status zr_skipreduce(void* const* bufs, int32_t n, int64_t m, zr_dtype dt,
                         const zr_skip_cfg* cfg, void* stream);
+
+/*
+ * Selective SkipReduce: several gradient buckets in one launch [SR section
+ * 4.4: gradients are communicated in buckets, each its own AllReduce, so
+ * each bucket can take its own skip rate -- aggressive for unimportant
+ * layers, k = 0 for protected ones].
+ *
+ * buckets    host array of n_buckets entries, 1 <= n_buckets <=
+ *            ZR_MAX_BUCKETS and n_buckets * n <= ZR_MAX_BUCKET_BUFS.
+ *            Bucket b is bufs (host array of n device pointers, each
+ *            16-byte aligned), m elements per rank buffer (>= 0) and its own
+ *            zr_skip_cfg (mode, k, seed, step, divisor, flags), validated as
+ *            for zr_skipreduce.  No two buffers of any buckets may overlap.
+ * n, dt      ranks and element type, shared by every bucket.
+ * Result: every bucket ends exactly as zr_skipreduce(bucket.bufs, n,
+ * bucket.m, dt, &bucket.cfg) would leave it, bit for bit.  The caller gives
+ * each bucket its own seed or step when buckets should skip different
+ * slices.
+ */
+#define ZR_MAX_BUCKETS 128
+#define ZR_MAX_BUCKET_BUFS 2048
+
+typedef struct zr_bucket {
+  void* const* bufs;
+  int64_t m;
+  zr_skip_cfg cfg;
+} zr_bucket;
+
+zr_status zr_skipreduce_buckets(const zr_bucket* buckets, int32_t n_buckets, int32_t n,
+                                zr_dtype dt, void* stream);
+
+/*
+ * AllReduce_Dropout, in place [SR section 4.2, Algorithm 1 "AllReduce with
+ * Fine-Grained Skipping": at every Reduce-Scatter step the receiving rank
+ * skips its local gradient element with probability p, forwarding what it
+ * received unchanged; the AllGather is the baseline one].
+ *
+ * Arguments as zr_ring_allreduce, plus:
+ * threshold  T in [0, 2^32]: an element is skipped when its 32-bit draw is
+ *            below T; T = ceil(p * 2^32) gives skip probability p (T = 0
+ *            never skips, T = 2^32 always does).
+ * seed, step generator seed shared by every rank, and the iteration count.
+ * Draw of receiving rank r for element e (its index in the buffer): the high
+ * 32 bits of output number e of SplitMix64 seeded with
+ * s_r = (output number step * 64 + r of SplitMix64 seeded with seed).
+ * Result: slice c (as in zr_ring_allreduce) is folded from its first sender,
+ * rank c, whose value is always kept; rank c + t (t = 1 .. n-1, mod n) adds
+ * its value unless its draw for e is below T.  Then divided by n when
+ * average = 1, (bf16) rounded once, and written to every rank.  Every rank's
+ * element is read (skipping saves no traffic, as the pages note).
+ */
+zr_status zr_allreduce_dropout(void* const* bufs, int32_t n, int64_t m, zr_dtype dt,
+                               uint64_t threshold, uint64_t seed, uint64_t step,
+                               int32_t average, void* stream);
 
 /*
  * Sparse (COO) aggregation with partitioning [ZEN section 2.1 (COO), Problem

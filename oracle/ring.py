@@ -107,8 +107,8 @@ def dropout_skips(seed, step, r, elems, threshold):
     below ``threshold`` (an integer in [0, 2**32]).
     """
     s = dropout_stream(seed, step, r)
-    elems = np.asarray(elems, dtype=np.int64)
-    return np.array([(splitmix.output(s, int(e)) >> 32) < threshold for e in elems], dtype=bool)
+    draws = splitmix.outputs(s, np.asarray(elems, dtype=np.int64)) >> np.uint64(32)
+    return draws.astype(np.int64) < threshold
 
 
 def ring_allreduce(x, k=0, o=0, divisor=DIV_NONE, chunk=None, counters=None, dropout=None,

@@ -36,6 +36,19 @@ def output(seed, i):
     return mix64((seed + (i + 1) * GAMMA) & MASK64)
 
 
+def outputs(seed, indices):
+    """``output(seed, i)`` for every i of an integer array, in numpy uint64
+    arithmetic (which wraps mod 2**64, as the definition does)."""
+    import numpy as np
+
+    i = np.asarray(indices, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = np.uint64(seed & MASK64) + (i + np.uint64(1)) * np.uint64(GAMMA)
+        z = (z ^ (z >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+        z = (z ^ (z >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+        return z ^ (z >> np.uint64(31))
+
+
 def sequence(seed, count):
     """The first ``count`` outputs, by stepping the state (not by ``output``)."""
     state = seed & MASK64

@@ -86,8 +86,51 @@ def test_dense_argument_errors_before_launch(zr):
         cfg = zr.SkipCfg(zr.ZR_SKIP_STATIC, k, 0, 0, zr.ZR_DIV_N, 0)
         assert zr.zr_skipreduce(fake, 2, 16, zr.ZR_F32, cfg, None) == zr.ZR_ERR_INVALID_ARG
     for bad in (zr.SkipCfg(5, 1, 0, 0, zr.ZR_DIV_N, 0), zr.SkipCfg(0, 1, 0, 0, 9, 0),
-                zr.SkipCfg(0, 1, 0, 0, zr.ZR_DIV_N, 1)):
+                zr.SkipCfg(0, 1, 0, 0, zr.ZR_DIV_N, 2)):
         assert zr.zr_skipreduce(fake, 2, 16, zr.ZR_F32, bad, None) == zr.ZR_ERR_INVALID_ARG
+
+
+def test_bucket_and_dropout_argument_errors_before_launch(zr):
+    # Made-up pointers on a machine without a GPU: every call below must be
+    # refused on the host, before anything could be launched.
+    a = [1 << 40, (1 << 40) + (1 << 30)]
+    b = [(1 << 40) + (2 << 30), (1 << 40) + (3 << 30)]
+    ok = zr.SkipCfg(zr.ZR_SKIP_RANDOM, 1, 0, 0, zr.ZR_DIV_N, 0)
+    bad_flags = zr.SkipCfg(zr.ZR_SKIP_RANDOM, 1, 0, 0, zr.ZR_DIV_N, 4)
+    bad_k = zr.SkipCfg(zr.ZR_SKIP_RANDOM, 2, 0, 0, zr.ZR_DIV_N, 0)
+    f32 = zr.ZR_F32
+    assert zr.zr_skipreduce_buckets([], 2, f32, None) == zr.ZR_ERR_INVALID_ARG
+    assert zr.zr_skipreduce_buckets([(a, 16, ok)], 0, f32, None) == zr.ZR_ERR_INVALID_ARG
+    assert zr.zr_skipreduce_buckets([(a, 16, ok)] * 129, 2, f32, None) == zr.ZR_ERR_INVALID_ARG
+    assert zr.zr_skipreduce_buckets([(a, 16, bad_flags)], 2, f32, None) == zr.ZR_ERR_INVALID_ARG
+    assert zr.zr_skipreduce_buckets([(a, 16, ok), (b, 16, bad_k)], 2, f32, None) == zr.ZR_ERR_INVALID_ARG
+    # buffers of two buckets overlapping each other
+    assert zr.zr_skipreduce_buckets([(a, 16, ok), ([a[0] + 32, b[0]], 16, ok)], 2, f32,
+                                    None) == zr.ZR_ERR_INVALID_ARG
+    assert zr.zr_skipreduce_buckets([(a, 16, ok), ([b[0] + 8, b[1]], 16, ok)], 2, f32,
+                                    None) == zr.ZR_ERR_ALIGNMENT
+    # every bucket empty: a valid no-op
+    assert zr.zr_skipreduce_buckets([(a, 0, ok), (b, 0, ok)], 2, f32, None) == zr.ZR_OK
+    # 32 buckets of 64 ranks fill the 2048-pointer table; one more bucket does not fit
+    many = [[(1 << 40) + ((j * 64 + r) << 20) for r in range(64)] for j in range(33)]
+    cfg0 = zr.SkipCfg(zr.ZR_SKIP_STATIC, 0, 0, 0, zr.ZR_DIV_N, 0)
+    assert zr.zr_skipreduce_buckets([(p, 0, cfg0) for p in many[:32]], 64, f32, None) == zr.ZR_OK
+    assert zr.zr_skipreduce_buckets([(p, 0, cfg0) for p in many], 64, f32,
+                                    None) == zr.ZR_ERR_INVALID_ARG
+    dr = zr.zr_allreduce_dropout
+    assert dr(a, 2, 16, f32, (1 << 32) + 1, 0, 0, 1, None) == zr.ZR_ERR_INVALID_ARG
+    assert dr(a, 2, 16, f32, 0, 0, 0, 2, None) == zr.ZR_ERR_INVALID_ARG
+    assert dr(a, 0, 16, f32, 0, 0, 0, 1, None) == zr.ZR_ERR_INVALID_ARG
+    assert dr([a[0] + 4, a[1]], 2, 16, f32, 0, 0, 0, 1, None) == zr.ZR_ERR_ALIGNMENT
+    assert dr(a, 2, 0, f32, 1 << 32, 0, 0, 1, None) == zr.ZR_OK
+
+
+def test_dropout_threshold_wrapper_matches_oracle():
+    import gradient_synchronisation_gb300 as g
+    from oracle import ring
+
+    for p in (0.0, 1.0, 0.5, 0.1, 1e-9, 0.999999, 2.0 ** -32):
+        assert g.dropout_threshold(p) == ring.dropout_threshold(p)
 
 
 def test_sparse_argument_errors_before_launch(zr):

@@ -79,3 +79,16 @@ def test_range_reduce_bounds():
     for n in (1, 2, 3, 8, 16, 64):
         assert splitmix.range_reduce(0, n) == 0
         assert splitmix.range_reduce((1 << 32) - 1, n) == n - 1
+
+
+def test_vectorised_outputs_equal_scalar_definition():
+    import numpy as np
+
+    from oracle import splitmix as sm
+
+    rng = np.random.default_rng(5)
+    for seed in (0, 1, 0x9E3779B97F4A7C15, (1 << 64) - 1, 123456789):
+        idx = np.concatenate([np.arange(40), rng.integers(0, 1 << 40, size=200)])
+        got = sm.outputs(seed, idx)
+        want = [sm.output(seed, int(i)) for i in idx]
+        assert [int(v) for v in got] == want
