@@ -67,7 +67,8 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=("ring", "skip", "sparse", "partition"), default=None,
+    ap.add_argument("--only", choices=("ring", "skip", "sparse", "partition", "dropout", "buckets"),
+                    default=None,
                     help="profiling: time one component alone (prints a profiling line, not the "
                          "benchmark line)")
     ap.add_argument("--dense-m", type=int, default=None,
@@ -195,7 +196,7 @@ class Workload:
         self.n, self.k = c2["n"], c2["skip_k"]
         self.m = dense_m or c2["m"]
         self.seed = c2["skip_seed"]
-        self.dense_on = any(c in self.components for c in ("ring", "skip"))
+        self.dense_on = any(c in self.components for c in ("ring", "skip", "dropout", "buckets"))
         self.sparse_on = any(c in self.components for c in ("sparse", "partition"))
         if self.dense_on:
             if dense_m:
@@ -204,6 +205,16 @@ class Workload:
                 self.host_dense = workloads.dense_c2()
             self.dense = torch.from_numpy(self.host_dense).to(dev)
             self.bufs = [self.dense[r] for r in range(self.n)]
+            # Selective SkipReduce: the flat gradient in 25 MB buckets (the
+            # DDP default size), the first bucket protected (k = 0), the
+            # others skipping k Reduce-Scatter steps (Random mode).
+            bucket = 25 * (1 << 20) // 4
+            self.buckets = []
+            for b, lo in enumerate(range(0, self.m, bucket)):
+                hi = min(lo + bucket, self.m)
+                self.buckets.append(dict(bufs=[self.dense[r, lo:hi] for r in range(self.n)],
+                                         k=0 if b == 0 else self.k, mode=zr.ZR_SKIP_RANDOM,
+                                         seed=self.seed + b, step=0, m=hi - lo))
         if self.sparse_on:
             cfg = workloads.SPARSE_C4 if sparse == "c4" else workloads.DGC_C5B
             self.m4, self.parts = cfg["m"], cfg["n_parts"]
@@ -233,6 +244,9 @@ class Workload:
         if self.dense_on:
             out["ring"] = 2 * self.n * self.m * s
             out["skip"] = (self.n - self.k) * self.m * s + self.n * self.m * s
+            out["dropout"] = 2 * self.n * self.m * s
+            out["buckets"] = sum((self.n - b["k"]) * b["m"] * s + self.n * b["m"] * s
+                                 for b in self.buckets)
         if self.sparse_on:
             out["sparse"] = sum(self.nnz) * 8 + self.union * 8 + (self.parts + 1) * 8 + 8
             out["partition"] = self.nnz[0] * 8 * 2 + (self.parts + 1) * 8
@@ -244,6 +258,11 @@ class Workload:
             zr.ring_allreduce(self.bufs, average=True)
         elif name == "skip":
             zr.skipreduce(self.bufs, k=self.k, mode=zr.ZR_SKIP_RANDOM, seed=self.seed, step=i)
+        elif name == "dropout":
+            zr.allreduce_dropout(self.bufs, 0.5, seed=self.seed, step=i)
+        elif name == "buckets":
+            zr.skipreduce_buckets([{k: v for k, v in dict(b, step=i).items() if k != "m"}
+                                   for b in self.buckets])
         elif name == "sparse":
             zr.sparse_aggregate(self.d_idx, self.d_val, self.m4, self.parts, self.part_seed,
                                 work=self.work)
