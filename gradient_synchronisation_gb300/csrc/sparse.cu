@@ -783,6 +783,9 @@ PartLayout part_layout(int64_t tiles, int parts) {
   return L;
 }
 
+// kIdentity: the input is the index range itself (position i holds index i,
+// no values) -- the partition that builds Zen's index sets I_p.
+template <bool kIdentity>
 __global__ void __launch_bounds__(kPartThreads)
 part_count_kernel(const int32_t* idx, int64_t nnz, int64_t tiles, H0 h, int parts,
                   int32_t* cnt_g, unsigned long long* seg_g, unsigned long long* tot_g) {
@@ -795,7 +798,7 @@ part_count_kernel(const int32_t* idx, int64_t nnz, int64_t tiles, H0 h, int part
     const int64_t lo = t * kPartTile, hi = min(lo + kPartTile, nnz);
     for (int64_t i = lo + tid; i < lo + kPartTile; i += kPartThreads) {
       const bool live = i < hi;
-      const int p = live ? (int)hash((uint32_t)idx[i]) : parts;
+      const int p = live ? (int)hash(kIdentity ? (uint32_t)i : (uint32_t)idx[i]) : parts;
       const unsigned peers = __match_any_sync(0xffffffffu, p);
       if (live && (peers & lanemask_lt()) == 0) atomicAdd(&cnt[p], __popc(peers));
     }
@@ -807,6 +810,7 @@ part_count_kernel(const int32_t* idx, int64_t nnz, int64_t tiles, H0 h, int part
 
 // Each warp owns kPartTile / warps consecutive entries of the tile and walks
 // them 32 at a time, so the entries of one partition leave in input order.
+template <bool kIdentity>
 __global__ void __launch_bounds__(kPartThreads)
 part_write_kernel(const int32_t* idx, const float* val, int64_t nnz, int64_t tiles, H0 h,
                   int parts, const int32_t* cnt_g, const unsigned long long* seg_g,
@@ -830,7 +834,7 @@ part_write_kernel(const int32_t* idx, const float* val, int64_t nnz, int64_t til
     for (int j = 0; j < kPerWarp; j += 32) {
       const int64_t i = lo + j + lane;
       const bool live = i < hi;
-      const int p = live ? (int)hash((uint32_t)idx[i]) : parts;
+      const int p = live ? (int)hash(kIdentity ? (uint32_t)i : (uint32_t)idx[i]) : parts;
       const unsigned peers = __match_any_sync(0xffffffffu, p);
       if (live && (peers & lanemask_lt()) == 0) wbase[warp * parts + p] += __popc(peers);
       __syncwarp();
@@ -848,13 +852,13 @@ part_write_kernel(const int32_t* idx, const float* val, int64_t nnz, int64_t til
     for (int j = 0; j < kPerWarp; j += 32) {
       const int64_t i = lo + j + lane;
       const bool live = i < hi;
-      const int32_t key = live ? idx[i] : 0;
+      const int32_t key = live ? (kIdentity ? (int32_t)i : idx[i]) : 0;
       const int p = live ? (int)hash((uint32_t)key) : parts;
       const unsigned peers = __match_any_sync(0xffffffffu, p);
       if (live) {
         const long long dst = wbase[warp * parts + p] + __popc(peers & lanemask_lt());
         out_idx[dst] = key;
-        out_val[dst] = val[i];
+        if (!kIdentity) out_val[dst] = val[i];
       }
       __syncwarp();
       if (live && (peers & lanemask_lt()) == 0) wbase[warp * parts + p] += __popc(peers);
@@ -897,7 +901,7 @@ DeviceInfo* device_info() {
                              write_max) != cudaSuccess)
       return nullptr;
     d.count_per_sm = per_sm((const void*)bin_count_kernel, kBinThreads, 0);
-    d.part_count_per_sm = per_sm((const void*)part_count_kernel, kPartThreads, 0);
+    d.part_count_per_sm = per_sm((const void*)part_count_kernel<false>, kPartThreads, 0);
     d.ready = 1;
   }
   return &d;
@@ -978,9 +982,11 @@ size_t partition_workspace_bytes(int64_t nnz, int n_parts) {
   return part_layout(tiles, n_parts).total;
 }
 
-zr_status partition_launch(const int32_t* idx, const float* val, int64_t nnz, int n_parts,
-                           uint64_t part_seed, int32_t* out_idx, float* out_val,
-                           int64_t* d_offsets, void* ws, cudaStream_t stream) {
+namespace {
+template <bool kIdentity>
+zr_status partition_run(const int32_t* idx, const float* val, int64_t nnz, int n_parts,
+                        uint64_t part_seed, int32_t* out_idx, float* out_val,
+                        int64_t* d_offsets, void* ws, cudaStream_t stream) {
   const int64_t tiles = (nnz + kPartTile - 1) / kPartTile;
   const PartLayout L = part_layout(tiles, n_parts);
   unsigned char* w = static_cast<unsigned char*>(ws);
@@ -996,12 +1002,27 @@ zr_status partition_launch(const int32_t* idx, const float* val, int64_t nnz, in
   DeviceInfo* dinfo = device_info();
   if (!dinfo) return ZR_ERR_CUDA;
   if (cudaMemsetAsync(w, 0, L.cnt, stream) != cudaSuccess) return ZR_ERR_CUDA;
-  part_count_kernel<<<(unsigned)grid_for(tiles, dinfo->part_count_per_sm), kPartThreads, 0,
+  part_count_kernel<kIdentity><<<(unsigned)grid_for(tiles, dinfo->part_count_per_sm), kPartThreads, 0,
                       stream>>>(idx, nnz, tiles, h, n_parts, cnt, seg, tot);
   const size_t smem = (size_t)(kPartThreads / 32) * n_parts * sizeof(long long);
-  part_write_kernel<<<(unsigned)grid_for(tiles, 4), kPartThreads, smem, stream>>>(
+  part_write_kernel<kIdentity><<<(unsigned)grid_for(tiles, 4), kPartThreads, smem, stream>>>(
       idx, val, nnz, tiles, h, n_parts, cnt, seg, tot, out_idx, out_val, d_offsets);
   return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
+}
+
+}  // namespace
+
+zr_status partition_launch(const int32_t* idx, const float* val, int64_t nnz, int n_parts,
+                           uint64_t part_seed, int32_t* out_idx, float* out_val,
+                           int64_t* d_offsets, void* ws, cudaStream_t stream) {
+  return partition_run<false>(idx, val, nnz, n_parts, part_seed, out_idx, out_val, d_offsets, ws,
+                              stream);
+}
+
+zr_status index_sets_launch(int64_t m, int n_parts, uint64_t part_seed, int32_t* out_sets,
+                            int64_t* d_offsets, void* ws, cudaStream_t stream) {
+  return partition_run<true>(nullptr, nullptr, m, n_parts, part_seed, out_sets, nullptr, d_offsets,
+                             ws, stream);
 }
 
 }  // namespace zr

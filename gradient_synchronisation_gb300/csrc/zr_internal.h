@@ -29,6 +29,22 @@ zr_status sparse_launch(const int32_t* const* idx, const float* const* val, cons
                         int32_t* out_idx, float* out_val, int64_t out_cap, int64_t* d_out_nnz,
                         int64_t* d_offsets, void* ws, cudaStream_t stream);
 
+// Zen's index sets I_p (the partition of [0, m) by h0); same workspace as a
+// partition of m entries.
+zr_status index_sets_launch(int64_t m, int n_parts, uint64_t part_seed, int32_t* out_sets,
+                            int64_t* d_offsets, void* ws, cudaStream_t stream);
+
+// Hash bitmap encode / decode; arguments already validated.
+size_t hash_bitmap_workspace_bytes(int64_t m, int n_parts);
+zr_status hash_bitmap_encode_launch(const int32_t* sets, const int64_t* d_set_offsets, int64_t m,
+                                    int n_parts, const int32_t* keys, int64_t n_keys,
+                                    uint32_t* out_bits, int64_t out_cap_words,
+                                    int64_t* d_word_offsets, void* ws, cudaStream_t stream);
+zr_status hash_bitmap_decode_launch(const int32_t* sets, const int64_t* d_set_offsets, int64_t m,
+                                    int n_parts, const uint32_t* bits, int32_t* out_keys,
+                                    int64_t out_cap, int64_t* d_key_offsets, void* ws,
+                                    cudaStream_t stream);
+
 // Push-side partition; arguments already validated.
 size_t partition_workspace_bytes(int64_t nnz, int n_parts);
 zr_status partition_launch(const int32_t* idx, const float* val, int64_t nnz, int n_parts,

@@ -260,6 +260,74 @@ zr_status zr_partition(const int32_t* idx, const float* val, int64_t nnz,
 size_t zr_partition_workspace_size(int64_t nnz, int32_t n_parts);
 
 /*
+ * Zen's index sets [ZEN section 3.3.2 "Hash bitmap": the indices a worker
+ * pushes to server p are I_p = {x in [0, M) : h0(x) = p}, computed once,
+ * offline, and sorted].
+ *
+ * dense_size M, 1 <= M <= 2^31 - 1.   n_parts: 1 <= n_parts <= ZR_MAX_PARTS.
+ * out_sets   device int32[M]: every I_p, ascending, concatenated in
+ *            partition order (a permutation of 0 .. M-1).
+ * d_offsets  device int64[n_parts + 1]: I_p = out_sets[d_offsets[p] ..
+ *            d_offsets[p+1]).
+ * ws         device workspace of zr_partition_workspace_size(M, n_parts)
+ *            bytes, 16-byte aligned.
+ * h0 is the partition hash of zr_sparse_aggregate (same part_seed).
+ */
+zr_status zr_hash_index_sets(int64_t dense_size, int32_t n_parts, uint64_t part_seed,
+                             int32_t* out_sets, int64_t* d_offsets, void* ws, size_t ws_bytes,
+                             void* stream);
+
+/*
+ * Hash bitmap encode [ZEN section 3.3.2, Figure 10, Algorithm 2
+ * hash_bitmap_encode: a server marks which elements of I_p are nonzero,
+ * one bit each, so that all servers' bitmaps total |G| bits].
+ *
+ * sets, d_set_offsets  the index sets from zr_hash_index_sets (device).
+ * dense_size, n_parts  as there.
+ * keys, n_keys   device int32: the nonzero indices (any order, each in
+ *                [0, M)), e.g. the out_idx of zr_sparse_aggregate.
+ * out_bits       device uint32[out_cap_words], out_cap_words >=
+ *                ceil(M / 32) + n_parts.  Partition p's bitmap is
+ *                ceil(|I_p| / 32) words from word d_word_offsets[p]; bit j
+ *                (bit j mod 32 of word j / 32, least significant first) is 1
+ *                iff I_p[j] is one of the keys; padding bits are 0.
+ * d_word_offsets device int64[n_parts + 1] (output).
+ * ws             device workspace of zr_hash_bitmap_workspace_size(M,
+ *                n_parts) bytes, 16-byte aligned; its first 4 bytes are the
+ *                status word (ZR_ERR_INPUT_UNSORTED: a key outside [0, M);
+ *                ZR_ERR_INVALID_ARG: offsets or sets that are not index sets
+ *                of [0, M)).
+ */
+zr_status zr_hash_bitmap_encode(const int32_t* sets, const int64_t* d_set_offsets,
+                                int64_t dense_size, int32_t n_parts, const int32_t* keys,
+                                int64_t n_keys, uint32_t* out_bits, int64_t out_cap_words,
+                                int64_t* d_word_offsets, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Hash bitmap decode [ZEN section 3.3.2, Algorithm 2 hash_bitmap_decode: a
+ * worker maps the set bits j of server p's bitmap back to the indices
+ * I_p[j]].
+ *
+ * bits           device uint32 bitmaps laid out as zr_hash_bitmap_encode
+ *                writes them (partition p from word sum_{q<p} ceil(|I_q|/32)).
+ * out_keys       device int32[out_cap]: partition-major, ascending inside a
+ *                partition (the indices I_p[j] of the set bits j).
+ * d_key_offsets  device int64[n_parts + 1] (output): partition p's keys are
+ *                out_keys[d_key_offsets[p] .. d_key_offsets[p+1]).
+ * ws             as for encode.  Status: ZR_ERR_CAPACITY if more keys than
+ *                out_cap (nothing is written past it), ZR_ERR_INVALID_ARG if a
+ *                padding bit is set or the sets are not index sets of [0, M).
+ */
+zr_status zr_hash_bitmap_decode(const int32_t* sets, const int64_t* d_set_offsets,
+                                int64_t dense_size, int32_t n_parts, const uint32_t* bits,
+                                int32_t* out_keys, int64_t out_cap, int64_t* d_key_offsets,
+                                void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes zr_hash_bitmap_encode / _decode need (0 on invalid
+ * arguments). */
+size_t zr_hash_bitmap_workspace_size(int64_t dense_size, int32_t n_parts);
+
+/*
  * zr_partition without a workspace argument, for callers that cannot
  * allocate device memory (for example a gradient hook running inside a
  * framework whose caching allocator owns the device, or a service that

@@ -41,9 +41,9 @@ def encode(index_set, nonzero):
     ``nonzero``.  Returns uint32 words."""
     index_set = np.asarray(index_set, dtype=np.int64)
     present = np.isin(index_set, np.asarray(nonzero, dtype=np.int64))
+    j = np.nonzero(present)[0]
     out = np.zeros(words(index_set.size), dtype=np.uint64)
-    for j in np.nonzero(present)[0]:
-        out[j // 32] |= np.uint64(1) << np.uint64(j % 32)
+    np.bitwise_or.at(out, j // 32, np.uint64(1) << (j % 32).astype(np.uint64))
     return out.astype(np.uint32)
 
 
@@ -51,8 +51,9 @@ def decode(index_set, bitmap):
     """Indices index_set[j] for every set bit j, ascending in j."""
     index_set = np.asarray(index_set, dtype=np.int32)
     bitmap = np.asarray(bitmap, dtype=np.uint32)
-    js = [j for j in range(index_set.size) if (int(bitmap[j // 32]) >> (j % 32)) & 1]
-    return index_set[np.array(js, dtype=np.int64)]
+    j = np.arange(index_set.size, dtype=np.int64)
+    bit = (bitmap[j // 32] >> (j % 32).astype(np.uint32)) & np.uint32(1)
+    return index_set[bit == 1]
 
 
 def encode_all(m, n_parts, seed, nonzero):
