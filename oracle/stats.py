@@ -12,6 +12,12 @@ with Sparsity-driven Data Synchronization":
   [i*ceil(M/n), (i+1)*ceil(M/n)));
 * Push and Pull imbalance ratios, Definition 8:
   max_{i,j} n*|I_i^j| / |I_i| and max_j n*|I'_j| / |I|.
+* the scheme choice of section 2.3 (Theorem 1, Equations (1) and (2)):
+  balanced parallelism moves 2(n-1)(gamma_n + 1) d_G M / n per GPU,
+  hierarchical centralisation 2 sum_{i=1}^{log n} gamma_{2^(i-1)} d_G M.
+  The pages take n a power of two and one average densification ratio per
+  group size; here gamma_k is the mean over the n/k groups of k consecutive
+  ranks (the groups the hierarchy merges), over the mean per-rank count.
 """
 
 import numpy as np
@@ -60,3 +66,42 @@ def push_imbalance(idx_lists, part_of, n):
 def pull_imbalance(union_idx, part_of, n):
     counts = np.bincount(part_of(np.asarray(union_idx)), minlength=n)
     return n * counts.max() / len(union_idx)
+
+
+def group_union_counts(idx_lists):
+    """For L = 0 .. log2(n): the sum over the n / 2^L groups of 2^L
+    consecutive ranks of the size of the group's union (Python sets)."""
+    n = len(idx_lists)
+    if n & (n - 1):
+        raise ValueError("n must be a power of two")
+    sets = [set(int(v) for v in a) for a in idx_lists]
+    out = []
+    g = 1
+    while g <= n:
+        total = 0
+        for start in range(0, n, g):
+            u = set()
+            for r in range(start, start + g):
+                u |= sets[r]
+            total += len(u)
+        out.append(total)
+        g *= 2
+    return out
+
+
+def gammas_from_counts(union_counts, total_nnz, n):
+    """gamma_{2^L} = (mean union of a 2^L group) / (mean per-rank count)."""
+    return [union_counts[level] * (1 << level) / total_nnz for level in range(len(union_counts))]
+
+
+BALANCED_PARALLELISM = 0
+HIERARCHICAL_CENTRALISATION = 1
+
+
+def choose_scheme(gammas, n):
+    """Equations (1) and (2) without the common factor d_G M / b; the
+    balanced scheme is kept on a tie.  Returns (choice, t_bp, t_hc)."""
+    logn = n.bit_length() - 1
+    t_bp = 2 * (n - 1) * (gammas[logn] + 1) / n
+    t_hc = 2 * sum(gammas[i - 1] for i in range(1, logn + 1))
+    return (BALANCED_PARALLELISM if t_bp <= t_hc else HIERARCHICAL_CENTRALISATION), t_bp, t_hc

@@ -166,3 +166,53 @@ def test_c4_generator_statistics():
     u_cold = (cold - 67_109) * (1 - (1 - 67_109 / (cold - 67_109)) ** n)
     gamma = (pool + u_hot + u_cold) / 335_544
     assert stats.densification_ratio(idx_l, m) == pytest.approx(gamma, rel=2e-3)
+
+
+# --------------------------------------------------------- scheme choice
+def test_group_union_counts_brute_force():
+    from oracle import stats
+
+    rng = np.random.default_rng(31)
+    for n in (1, 2, 4, 8):
+        lists = [np.unique(rng.integers(0, 200, size=rng.integers(0, 60))) for _ in range(n)]
+        counts = stats.group_union_counts(lists)
+        assert counts[0] == sum(len(a) for a in lists)
+        assert counts[-1] == len(set().union(*[set(a.tolist()) for a in lists]))
+        # each level: sum over groups, recomputed by hand
+        for level, c in enumerate(counts):
+            g = 1 << level
+            want = sum(len(set(np.concatenate(lists[s:s + g]).tolist())) for s in range(0, n, g))
+            assert c == want
+
+
+@pytest.mark.parametrize("n", [4, 8, 16, 64])
+def test_scheme_choice_extreme_cases(n):
+    # Zen section 2.3: with full overlap (gamma_k = 1) the hierarchical sum
+    # is log n while the balanced term is 2(n-1)/n < 2, so balanced
+    # parallelism wins; with no overlap (gamma_k = k) the sum is n - 1 and
+    # the balanced term (n-1)(1 + 1/n) is larger, so the hierarchy wins.
+    from oracle import stats
+
+    logn = n.bit_length() - 1
+    full = [1.0] * (logn + 1)
+    choice, t_bp, t_hc = stats.choose_scheme(full, n)
+    assert t_hc == pytest.approx(2 * logn) and t_bp == pytest.approx(4 * (n - 1) / n)
+    assert choice == stats.BALANCED_PARALLELISM
+    disjoint = [float(1 << level) for level in range(logn + 1)]
+    choice, t_bp, t_hc = stats.choose_scheme(disjoint, n)
+    assert t_hc == pytest.approx(2 * (n - 1)) and t_bp == pytest.approx(2 * (n - 1) * (1 + 1 / n))
+    assert choice == stats.HIERARCHICAL_CENTRALISATION
+
+
+def test_gammas_of_identical_and_disjoint_lists():
+    from oracle import stats
+
+    same = [np.arange(0, 100, 3)] * 8
+    g = stats.gammas_from_counts(stats.group_union_counts(same), 8 * 34, 8)
+    assert g == pytest.approx([1.0, 1.0, 1.0, 1.0])
+    disjoint = [np.arange(r * 50, r * 50 + 50) for r in range(8)]
+    g = stats.gammas_from_counts(stats.group_union_counts(disjoint), 400, 8)
+    assert g == pytest.approx([1.0, 2.0, 4.0, 8.0])
+    # gamma_n equals Definition 4's densification ratio
+    m = 1000
+    assert g[-1] == pytest.approx(stats.densification_ratio(disjoint, m))
