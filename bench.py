@@ -67,7 +67,8 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=("ring", "skip", "sparse", "partition", "dropout", "buckets"),
+    ap.add_argument("--only", choices=("ring", "skip", "sparse", "partition", "dropout", "buckets",
+                                       "hb_encode", "hb_decode"),
                     default=None,
                     help="profiling: time one component alone (prints a profiling line, not the "
                          "benchmark line)")
@@ -197,7 +198,8 @@ class Workload:
         self.m = dense_m or c2["m"]
         self.seed = c2["skip_seed"]
         self.dense_on = any(c in self.components for c in ("ring", "skip", "dropout", "buckets"))
-        self.sparse_on = any(c in self.components for c in ("sparse", "partition"))
+        self.sparse_on = any(c in self.components
+                             for c in ("sparse", "partition", "hb_encode", "hb_decode"))
         if self.dense_on:
             if dense_m:
                 self.host_dense = workloads.dense_f32_per_rank(self.n, self.m, c2["sigma"], 200)
@@ -237,6 +239,14 @@ class Workload:
                                 work=self.work)
             torch.cuda.synchronize()
             self.union = int(self.work.out_nnz.item())
+            if any(c in self.components for c in ("hb_encode", "hb_decode")):
+                # Zen's Pull: every server's hash bitmap of the union's keys
+                self.hb = zr.HashBitmap(self.m4, self.parts, self.part_seed)
+                self.hb_keys = self.work.out_idx[:self.union]
+                self.hb.encode(self.hb_keys)
+                self.hb_out = torch.empty(self.union, dtype=torch.int32, device=dev)
+                self.hb_koff = torch.empty(self.parts + 1, dtype=torch.int64, device=dev)
+                self.hb_bits = self.hb.bits.clone()
 
     def bytes(self):
         s = 4
@@ -250,6 +260,11 @@ class Workload:
         if self.sparse_on:
             out["sparse"] = sum(self.nnz) * 8 + self.union * 8 + (self.parts + 1) * 8 + 8
             out["partition"] = self.nnz[0] * 8 * 2 + (self.parts + 1) * 8
+            words = (self.m4 + 31) // 32
+            # encode: the index sets once, the keys once, the bitmaps out
+            out["hb_encode"] = self.m4 * 4 + self.union * 4 + words * 4
+            # decode: the bitmaps, the index-set entries of the set bits, the keys out
+            out["hb_decode"] = words * 4 + self.union * 4 * 2 + (self.parts + 1) * 8
         return {c: out[c] for c in self.components}
 
     def run(self, name, i):
@@ -263,6 +278,10 @@ class Workload:
         elif name == "buckets":
             zr.skipreduce_buckets([{k: v for k, v in dict(b, step=i).items() if k != "m"}
                                    for b in self.buckets])
+        elif name == "hb_encode":
+            self.hb.encode(self.hb_keys)
+        elif name == "hb_decode":
+            self.hb.decode(self.hb_bits, self.hb_out, self.hb_koff)
         elif name == "sparse":
             zr.sparse_aggregate(self.d_idx, self.d_val, self.m4, self.parts, self.part_seed,
                                 work=self.work)

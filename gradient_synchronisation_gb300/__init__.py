@@ -56,8 +56,11 @@ EXPORTS = (
     "zr_partition", "zr_partition_workspace_size", "zr_query_status", "zr_status_string",
     "zr_version", "zr_partition_static", "zr_skipreduce_buckets", "zr_allreduce_dropout",
     "zr_hash_index_sets", "zr_hash_bitmap_encode", "zr_hash_bitmap_decode",
-    "zr_hash_bitmap_workspace_size",
+    "zr_hash_bitmap_workspace_size", "zr_densification", "zr_densification_workspace_size",
+    "zr_choose_scheme",
 )
+ZR_SCHEME_BALANCED = 0
+ZR_SCHEME_HIERARCHICAL = 1
 ZR_STATIC_SCRATCH_BYTES = 2 << 20
 
 
@@ -104,6 +107,11 @@ def _load():
         "zr_hash_bitmap_encode": (i32, [P, P, i64, i32, P, i64, P, i64, P, P, sz, P]),
         "zr_hash_bitmap_decode": (i32, [P, P, i64, i32, P, P, i64, P, P, sz, P]),
         "zr_hash_bitmap_workspace_size": (sz, [i64, i32]),
+        "zr_densification": (i32, [PP, ctypes.POINTER(i64), i32, i64, P, P, sz, P]),
+        "zr_densification_workspace_size": (sz, [i32, i64]),
+        "zr_choose_scheme": (i32, [ctypes.POINTER(i64), i32, ctypes.POINTER(ctypes.c_double),
+                                   ctypes.POINTER(ctypes.c_double),
+                                   ctypes.POINTER(ctypes.c_double)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -177,6 +185,27 @@ def zr_hash_bitmap_decode(sets, d_set_offsets, dense_size, n_parts, bits, out_ke
                           d_key_offsets, ws, ws_bytes, stream):
     return lib().zr_hash_bitmap_decode(sets, d_set_offsets, dense_size, n_parts, bits, out_keys,
                                        out_cap, d_key_offsets, ws, ws_bytes, stream)
+
+
+def zr_densification(idx, nnz, n, dense_size, d_union_counts, ws, ws_bytes, stream):
+    nnz_arr = (ctypes.c_int64 * max(1, len(nnz)))(*nnz)
+    return lib().zr_densification(_ptrs(idx), nnz_arr, n, dense_size, d_union_counts, ws,
+                                  ws_bytes, stream)
+
+
+def zr_densification_workspace_size(n, dense_size):
+    return lib().zr_densification_workspace_size(n, dense_size)
+
+
+def zr_choose_scheme(union_counts, n):
+    """Host call: returns (choice, gammas, t_bp, t_hc); choice -1 on invalid
+    arguments."""
+    levels = max(1, len(union_counts))
+    uc = (ctypes.c_int64 * levels)(*union_counts)
+    g = (ctypes.c_double * 8)()
+    bp, hc = ctypes.c_double(0), ctypes.c_double(0)
+    choice = lib().zr_choose_scheme(uc, n, g, ctypes.byref(bp), ctypes.byref(hc))
+    return choice, list(g)[:len(union_counts)], bp.value, hc.value
 
 
 def zr_sparse_aggregate(idx, val, nnz, n, dense_size, n_parts, part_seed, average, out_idx,
@@ -429,3 +458,30 @@ class HashBitmap:
 
     def status(self, stream=None):
         return zr_query_status(self.ws.data_ptr(), _stream(stream))
+
+
+def densification(idx_list, dense_size, stream=None):
+    """Union sizes of groups of 2^L consecutive ranks (int64 CUDA tensor of
+    log2(n) + 1 entries), measured on the device."""
+    import torch
+
+    n = len(idx_list)
+    nnz = [int(a.numel()) for a in idx_list]
+    dev = idx_list[0].device
+    ws_bytes = zr_densification_workspace_size(n, dense_size)
+    if ws_bytes == 0:
+        raise ValueError("densification needs a power-of-two rank count and a valid dense size")
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty(n.bit_length(), dtype=torch.int64, device=dev)
+    _check(zr_densification([a.data_ptr() for a in idx_list], nnz, n, dense_size, out.data_ptr(),
+                            ws.data_ptr(), ws_bytes, _stream(stream)), "zr_densification")
+    return out, ws
+
+
+def choose_scheme(union_counts, n):
+    """Zen's choice between balanced parallelism and hierarchical
+    centralisation from measured union sizes (host)."""
+    choice, g, bp, hc = zr_choose_scheme([int(v) for v in union_counts], n)
+    if choice < 0:
+        raise ValueError("invalid union counts or rank count")
+    return choice, g, bp, hc

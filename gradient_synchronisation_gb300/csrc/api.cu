@@ -183,6 +183,49 @@ zr_status zr_hash_bitmap_decode(const int32_t* sets, const int64_t* d_set_offset
                                        static_cast<cudaStream_t>(stream));
 }
 
+size_t zr_densification_workspace_size(int32_t n, int64_t dense_size) {
+  if (n < 1 || n > ZR_MAX_RANKS || (n & (n - 1)) != 0 || dense_size < 1 || dense_size > INT32_MAX)
+    return 0;
+  return zr::densify_workspace_bytes(n, dense_size);
+}
+
+zr_status zr_densification(const int32_t* const* idx, const int64_t* nnz, int32_t n,
+                           int64_t dense_size, int64_t* d_union_counts, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (!idx || !nnz || !d_union_counts) return ZR_ERR_INVALID_ARG;
+  if (n < 1 || n > ZR_MAX_RANKS || (n & (n - 1)) != 0) return ZR_ERR_INVALID_ARG;
+  if (dense_size < 1 || dense_size > INT32_MAX) return ZR_ERR_INVALID_ARG;
+  for (int r = 0; r < n; ++r) {
+    if (nnz[r] < 0 || nnz[r] > dense_size) return ZR_ERR_INVALID_ARG;
+    if (nnz[r] > 0 && !idx[r]) return ZR_ERR_INVALID_ARG;
+  }
+  zr_status st = zr::check_ws(ws, ws_bytes, zr::densify_workspace_bytes(n, dense_size));
+  if (st != ZR_OK) return st;
+  return zr::densify_launch(idx, nnz, n, dense_size, d_union_counts, ws,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int32_t zr_choose_scheme(const int64_t* union_counts, int32_t n, double* gammas, double* t_bp,
+                         double* t_hc) {
+  if (!union_counts || n < 2 || n > ZR_MAX_RANKS || (n & (n - 1)) != 0) return -1;
+  int logn = 0;
+  while ((1 << logn) < n) ++logn;
+  if (union_counts[0] <= 0) return -1;
+  double g[7];
+  for (int level = 0; level <= logn; ++level) {
+    if (union_counts[level] < 0) return -1;
+    g[level] = (double)union_counts[level] * (double)(1 << level) / (double)union_counts[0];
+    if (gammas) gammas[level] = g[level];
+  }
+  const double bp = 2.0 * (n - 1) * (g[logn] + 1.0) / n;
+  double hc = 0.0;
+  for (int i = 1; i <= logn; ++i) hc += g[i - 1];
+  hc *= 2.0;
+  if (t_bp) *t_bp = bp;
+  if (t_hc) *t_hc = hc;
+  return bp <= hc ? ZR_SCHEME_BALANCED : ZR_SCHEME_HIERARCHICAL;
+}
+
 size_t zr_sparse_workspace_size(int32_t n, int64_t dense_size, int32_t n_parts) {
   if (n < 1 || n > ZR_MAX_RANKS || dense_size < 1 || dense_size > INT32_MAX || n_parts < 0 ||
       n_parts > ZR_MAX_PARTS)

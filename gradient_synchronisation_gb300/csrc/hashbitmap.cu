@@ -14,7 +14,7 @@
 //           M bits (workspace; it stays in L2), then lane l of the warp tests
 //           element 32j + l of the word's index set and a ballot forms word j;
 //           the 32 words leave as one coalesced store.
-//   decode: per tile of 4096 words, a popcount pass and a one-CTA scan give
+//   decode: per tile of 1024 words, a popcount pass and a one-CTA scan give
 //           every tile its first output position; then each warp walks its
 //           words, and lane l of word j writes I_p[32j + l] (when bit l is
 //           set) at the word's base plus the popcount of the lower bits, so a
@@ -33,7 +33,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kTileWords = 4096;  // decode tile
+constexpr int kTileWords = 1024;  // decode tile
 constexpr int kScanThreads = 1024;
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -126,20 +126,36 @@ hb_encode_kernel(const int32_t* sets, const int64_t* set_off, int64_t m, int par
        g0 += nwarps * 32) {
     int p = word_part(s_woff, parts, g0, 0);
     uint32_t mine = 0;
-    for (int u = 0; u < 32; ++u) {
-      const int64_t g = g0 + u;
-      if (g >= total) break;  // the same for every lane
-      p = word_part(s_woff, parts, g, p);
-      const int64_t pos = (g - s_woff[p]) * 32 + lane;
-      const int64_t len = s_soff[p + 1] - s_soff[p];
-      bool bit = false;
-      if (pos < len) {
-        const int32_t x = sets[s_soff[p] + pos];
-        if (x >= 0 && x < m) bit = (mem[x >> 5] >> (x & 31)) & 1u;
-        else flag(status, ZR_ERR_INVALID_ARG);
+    for (int u0 = 0; u0 < 32; u0 += 8) {
+      if (g0 + u0 >= total) break;  // the same for every lane
+      // the index-set elements of 8 words first (8 loads in flight), then
+      // their membership bits, then the 8 ballots
+      int32_t x[8];
+      bool in[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t g = g0 + u0 + u;
+        in[u] = false;
+        x[u] = 0;
+        if (g < total) {
+          p = word_part(s_woff, parts, g, p);
+          const int64_t pos = (g - s_woff[p]) * 32 + lane;
+          if (pos < s_soff[p + 1] - s_soff[p]) {
+            x[u] = sets[s_soff[p] + pos];
+            in[u] = true;
+          }
+        }
       }
-      const uint32_t w = __ballot_sync(0xffffffffu, bit);
-      if (lane == u) mine = w;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        bool bit = false;
+        if (in[u]) {
+          if (x[u] >= 0 && x[u] < m) bit = (mem[x[u] >> 5] >> (x[u] & 31)) & 1u;
+          else flag(status, ZR_ERR_INVALID_ARG);
+        }
+        const uint32_t w = __ballot_sync(0xffffffffu, bit);
+        if (lane == u0 + u) mine = w;
+      }
     }
     if (g0 + lane < total) out[g0 + lane] = mine;
   }
@@ -208,14 +224,24 @@ hb_scan_kernel(const uint32_t* bits, const int64_t* woff_ws, int parts, const in
   }
   if (carry > out_cap && tid == 0) flag(status, ZR_ERR_CAPACITY);
   __syncthreads();
-  // key offset of partition p: the set bits before its first word
-  for (int p = tid; p <= parts; p += kScanThreads) {
+  // key offset of partition p: the set bits before its first word = its
+  // tile's base plus the popcount of the tile's words before it (the whole
+  // CTA sums those, one partition at a time)
+  for (int p = 0; p <= parts; ++p) {
     const int64_t w = woff_ws[p];
     const int64_t t = w / kTileWords;
-    long long k = t < tiles ? tbase[t] : carry;
+    int c = 0;
     if (t < tiles)
-      for (int64_t g = t * kTileWords; g < w; ++g) k += __popc(bits[g]);
-    key_off[p] = k;
+      for (int64_t g = t * kTileWords + tid; g < w; g += kScanThreads) c += __popc(bits[g]);
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (lane == 0) s_warp[warp] = c;
+    __syncthreads();
+    if (tid == 0) {
+      long long k = t < tiles ? tbase[t] : carry;
+      for (int i = 0; i < kScanThreads / 32; ++i) k += s_warp[i];
+      key_off[p] = k;
+    }
+    __syncthreads();
   }
 }
 
@@ -246,19 +272,31 @@ hb_decode_kernel(const int32_t* sets, const int64_t* set_off, int parts, const u
       const uint32_t mine = g0 + lane < whi ? bits[g0 + lane] : 0u;
       const int cnt = __popc(mine);
       const int incl = warp_incl_scan(cnt);
-      for (int u = 0; u < 32; ++u) {
-        const int64_t g = g0 + u;
-        if (g >= whi) break;  // the same for every lane
-        const uint32_t word = __shfl_sync(0xffffffffu, mine, u);
-        const int before = __shfl_sync(0xffffffffu, incl - cnt, u);
-        if (word == 0) continue;
-        p = word_part(s_woff, parts, g, p);
-        if ((word >> lane) & 1u) {
-          const int64_t pos = (g - s_woff[p]) * 32 + lane;
-          const int64_t dst = run + before + __popc(word & lt);
-          if (pos < s_soff[p + 1] - s_soff[p] && dst < out_cap) out[dst] = sets[s_soff[p] + pos];
-          else flag(status, ZR_ERR_INVALID_ARG);  // a bit past the set's end, or no room
+      {
+        constexpr int u0 = 0;
+        int32_t key[32];
+        int rel[32];  // output position relative to run; -1: nothing to write
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const int64_t g = g0 + u0 + u;
+          const uint32_t word = __shfl_sync(0xffffffffu, mine, u0 + u);
+          const int before = __shfl_sync(0xffffffffu, incl - cnt, u0 + u);
+          rel[u] = -1;
+          if (g < whi && ((word >> lane) & 1u)) {
+            p = word_part(s_woff, parts, g, p);
+            const int64_t pos = (g - s_woff[p]) * 32 + lane;
+            const int r = before + __popc(word & lt);
+            if (pos < s_soff[p + 1] - s_soff[p] && run + r < out_cap) {
+              key[u] = sets[s_soff[p] + pos];
+              rel[u] = r;
+            } else {
+              flag(status, ZR_ERR_INVALID_ARG);  // a bit past the set's end, or no room
+            }
+          }
         }
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+          if (rel[u] >= 0) out[run + rel[u]] = key[u];
       }
       run += __shfl_sync(0xffffffffu, incl, 31);
     }

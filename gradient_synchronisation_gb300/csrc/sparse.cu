@@ -868,6 +868,86 @@ part_write_kernel(const int32_t* idx, const float* val, int64_t nnz, int64_t til
   }
 }
 
+// ------------------------------------------------------------ densification
+// Union sizes of rank groups (Zen section 2.3, the densification ratios
+// gamma_k of Equations (1) and (2)).  Per bin, a warp ORs 1 << r into a
+// 64-bit holder mask per key for every entry of rank r; then, for every key
+// with a holder, level L folds the mask so that bit i * 2^L holds the OR of
+// group i's 2^L ranks, and the set bits at multiples of 2^L count the
+// groups of size 2^L whose union holds the key.  Sums per level stay in
+// registers until one atomic per warp at the end.
+constexpr int kDensWarps = 4;
+
+__device__ __forceinline__ unsigned long long group_sel(int level) {
+  switch (level) {
+    case 1: return 0x5555555555555555ull;
+    case 2: return 0x1111111111111111ull;
+    case 3: return 0x0101010101010101ull;
+    case 4: return 0x0001000100010001ull;
+    case 5: return 0x0000000100000001ull;
+    default: return 0x1ull;
+  }
+}
+
+__global__ void __launch_bounds__(kDensWarps * 32)
+densify_kernel(const __grid_constant__ Lists lists, int n, int logn, int log_w, int bins,
+               const int32_t* starts, int64_t total_nnz, unsigned long long* counts) {
+  extern __shared__ unsigned long long masks_all[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int W = 1 << log_w;
+  unsigned long long* mk = masks_all + (size_t)warp * W;
+  unsigned long long cnt[6] = {0, 0, 0, 0, 0, 0};
+  const int nwarps = gridDim.x * kDensWarps;
+  for (int b = blockIdx.x * kDensWarps + warp; b < bins; b += nwarps) {
+    const uint32_t base = (uint32_t)b << log_w;
+    for (int i = lane; i < W; i += 32) mk[i] = 0ull;
+    // lane r (and r + 32) holds rank r's slice of this bin
+    int lo[2], hi[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = lane + 32 * h;
+      lo[h] = hi[h] = 0;
+      if (r < n) {
+        const int32_t* row = starts + (size_t)r * (bins + 1) + b;
+        const int nnz = (int)lists.nnz[r];
+        lo[h] = min(max(__ldcg(row), 0), nnz);
+        hi[h] = min(max(__ldcg(row + 1), lo[h]), nnz);
+      }
+    }
+    __syncwarp();
+    for (int r = 0; r < n; ++r) {
+      const int a = __shfl_sync(0xffffffffu, r < 32 ? lo[0] : lo[1], r & 31);
+      const int e = __shfl_sync(0xffffffffu, r < 32 ? hi[0] : hi[1], r & 31);
+      const int32_t* ip = lists.idx[r];
+      for (int j = a + lane; j < e; j += 32) {
+        const uint32_t slot = (uint32_t)__ldg(ip + j) - base;
+        if (slot < (uint32_t)W) atomicOr(&mk[slot], 1ull << r);
+      }
+    }
+    __syncwarp();
+    for (int i = lane; i < W; i += 32) {
+      unsigned long long m = mk[i];
+      if (m) {
+#pragma unroll
+        for (int level = 1; level <= 6; ++level) {
+          if (level <= logn) {
+            m |= m >> (1 << (level - 1));
+            cnt[level - 1] += __popcll(m & group_sel(level));
+          }
+        }
+      }
+    }
+    __syncwarp();
+  }
+#pragma unroll
+  for (int level = 1; level <= 6; ++level) {
+    unsigned long long v = cnt[level - 1];
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0 && level <= logn && v) atomicAdd(&counts[level], v);
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(&counts[0], (unsigned long long)total_nnz);
+}
+
 // ------------------------------------------------------------ launch helpers
 int per_sm(const void* fn, int threads, size_t smem) {
   int b = 0;
@@ -974,6 +1054,66 @@ zr_status sparse_launch(const int32_t* const* idx, const float* const* val, cons
   bin_write_kernel<<<(unsigned)grid_for(write_units, o), kWriteThreads, smem, stream>>>(
       lists, n, g.log_w, bins, starts, h, parts, average, cnt, excl, tot, out_idx, out_val,
       out_cap, offsets_out, d_out_nnz, status);
+  return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
+}
+
+// Densification workspace: [status] then the bin starts (the sparse
+// layout's first region, with no partitions).
+size_t densify_workspace_bytes(int n, int64_t dense_size) {
+  const Geometry g = geometry(n, dense_size, 0, -1);
+  return sparse_layout(n, g.bins, 1).cnt;  // status + starts
+}
+
+zr_status densify_launch(const int32_t* const* idx, const int64_t* nnz, int n, int64_t dense_size,
+                         int64_t* d_union_counts, void* ws, cudaStream_t stream) {
+  Lists lists;
+  int64_t max_nnz = 0, total_nnz = 0;
+  for (int r = 0; r < ZR_MAX_RANKS; ++r) {
+    const bool live = r < n && nnz[r] > 0;
+    lists.idx[r] = live ? idx[r] : nullptr;
+    lists.val[r] = nullptr;
+    lists.nnz[r] = r < n ? nnz[r] : 0;
+    if (r < n) {
+      max_nnz = nnz[r] > max_nnz ? nnz[r] : max_nnz;
+      total_nnz += nnz[r];
+    }
+  }
+  int logn = 0;
+  while ((1 << logn) < n) ++logn;
+  const Geometry g = geometry(n, dense_size, 0, total_nnz);
+  const SparseLayout L = sparse_layout(n, g.bins, 1);
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(w);
+  int32_t* starts = reinterpret_cast<int32_t*>(w + L.starts);
+  const int bins = (int)g.bins;
+  if (cudaMemsetAsync(w, 0, L.starts, stream) != cudaSuccess) return ZR_ERR_CUDA;
+  if (cudaMemsetAsync(d_union_counts, 0, (size_t)(logn + 1) * 8, stream) != cudaSuccess)
+    return ZR_ERR_CUDA;
+  {
+    const int64_t groups = max_nnz / 4 + 1;
+    int64_t gx = (groups + 256 * kStartsUnroll - 1) / (256 * kStartsUnroll);
+    const int64_t cap = ((int64_t)sm_count() * 8 + n - 1) / n;
+    if (gx > cap) gx = cap;
+    if (gx < 1) gx = 1;
+    bin_starts_kernel<<<dim3((unsigned)gx, (unsigned)n), 256, 0, stream>>>(
+        lists, (int)dense_size, g.log_w, bins, starts, status);
+  }
+  const size_t smem = (size_t)kDensWarps * ((size_t)1 << g.log_w) * 8;
+  static bool attr_set[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ZR_ERR_CUDA;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(densify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)((size_t)kDensWarps * 4096 * 8)) != cudaSuccess)
+      return ZR_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  const int64_t units = (g.bins + kDensWarps - 1) / kDensWarps;
+  densify_kernel<<<(unsigned)grid_for(units, per_sm((const void*)densify_kernel, kDensWarps * 32,
+                                                      smem)),
+                   kDensWarps * 32, smem, stream>>>(lists, n, logn, g.log_w, bins, starts,
+                                                     total_nnz,
+                                                     reinterpret_cast<unsigned long long*>(d_union_counts));
   return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
 }
 

@@ -29,6 +29,11 @@ zr_status sparse_launch(const int32_t* const* idx, const float* const* val, cons
                         int32_t* out_idx, float* out_val, int64_t out_cap, int64_t* d_out_nnz,
                         int64_t* d_offsets, void* ws, cudaStream_t stream);
 
+// Union sizes of groups of 2^L consecutive ranks; arguments already validated.
+size_t densify_workspace_bytes(int n, int64_t dense_size);
+zr_status densify_launch(const int32_t* const* idx, const int64_t* nnz, int n, int64_t dense_size,
+                         int64_t* d_union_counts, void* ws, cudaStream_t stream);
+
 // Zen's index sets I_p (the partition of [0, m) by h0); same workspace as a
 // partition of m entries.
 zr_status index_sets_launch(int64_t m, int n_parts, uint64_t part_seed, int32_t* out_sets,

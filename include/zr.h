@@ -328,6 +328,47 @@ zr_status zr_hash_bitmap_decode(const int32_t* sets, const int64_t* d_set_offset
 size_t zr_hash_bitmap_workspace_size(int64_t dense_size, int32_t n_parts);
 
 /*
+ * Densification of rank groups, measured on the device [ZEN Definition 4
+ * and section 2.3: the densification ratio gamma_k of aggregating k sparse
+ * tensors decides between the two optimal schemes].
+ *
+ * idx, nnz, n, dense_size  as zr_sparse_aggregate (values are not needed);
+ *                n must be a power of two, 1 <= n <= ZR_MAX_RANKS.
+ * d_union_counts device int64[log2(n) + 1] (output): entry L is the sum,
+ *                over the n / 2^L groups of 2^L consecutive ranks
+ *                (ranks i*2^L .. (i+1)*2^L - 1), of the size of the union of
+ *                the group's index lists.  Entry 0 is sum(nnz); entry log2(n)
+ *                is the size of the whole union.
+ * ws, ws_bytes   device workspace of zr_densification_workspace_size(n,
+ *                dense_size) bytes, 16-byte aligned; status word first
+ *                (ZR_ERR_INPUT_UNSORTED as for zr_sparse_aggregate).
+ */
+zr_status zr_densification(const int32_t* const* idx, const int64_t* nnz, int32_t n,
+                           int64_t dense_size, int64_t* d_union_counts, void* ws,
+                           size_t ws_bytes, void* stream);
+
+size_t zr_densification_workspace_size(int32_t n, int64_t dense_size);
+
+/*
+ * Zen's scheme choice [ZEN Theorem 1 and Equations (1), (2)], on the host.
+ *
+ * union_counts  host int64[log2(n) + 1], as zr_densification writes them.
+ * gamma_k = union_counts[L] * k / union_counts[0] for k = 2^L (the mean
+ * union of a k-group over the mean per-rank count).  Balanced parallelism
+ * costs t_bp = 2 (n-1) (gamma_n + 1) / n, hierarchical centralisation
+ * t_hc = 2 sum_{i=1}^{log2 n} gamma_{2^(i-1)} (both in units of d_G M / b).
+ * gammas, t_bp, t_hc  optional host outputs (gammas has log2(n) + 1 slots).
+ * Returns ZR_SCHEME_BALANCED (also on a tie) or ZR_SCHEME_HIERARCHICAL, or
+ * -1 on invalid arguments (n not a power of two in [2, 64], a count < 0, or
+ * union_counts[0] = 0).
+ */
+#define ZR_SCHEME_BALANCED 0
+#define ZR_SCHEME_HIERARCHICAL 1
+
+int32_t zr_choose_scheme(const int64_t* union_counts, int32_t n, double* gammas, double* t_bp,
+                         double* t_hc);
+
+/*
  * zr_partition without a workspace argument, for callers that cannot
  * allocate device memory (for example a gradient hook running inside a
  * framework whose caching allocator owns the device, or a service that

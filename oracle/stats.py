@@ -74,17 +74,14 @@ def group_union_counts(idx_lists):
     n = len(idx_lists)
     if n & (n - 1):
         raise ValueError("n must be a power of two")
-    sets = [set(int(v) for v in a) for a in idx_lists]
+    lists = [np.unique(np.asarray(a, dtype=np.int64)) for a in idx_lists]
     out = []
     g = 1
     while g <= n:
         total = 0
         for start in range(0, n, g):
-            u = set()
-            for r in range(start, start + g):
-                u |= sets[r]
-            total += len(u)
-        out.append(total)
+            total += np.unique(np.concatenate(lists[start:start + g])).size
+        out.append(int(total))
         g *= 2
     return out
 

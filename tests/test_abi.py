@@ -7,6 +7,7 @@ import glob
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -164,3 +165,42 @@ def test_skip_fraction_to_k(zr):
         zr.skip_fraction_to_k(0.3, 8)
     with pytest.raises(ValueError):
         zr.skip_fraction_to_k(1.0, 8)
+
+
+def test_choose_scheme_host_call_matches_oracle(zr):
+    # zr_choose_scheme is plain host arithmetic: it runs here, without a GPU.
+    from oracle import stats
+
+    rng = np.random.default_rng(8)
+    for n in (2, 4, 8, 16, 32, 64):
+        logn = n.bit_length() - 1
+        for trial in range(50):
+            nnz_total = int(rng.integers(1, 10**7))
+            counts = [nnz_total]
+            for level in range(1, logn + 1):
+                counts.append(int(rng.integers(max(1, counts[-1] // 2), counts[-1] + 1)))
+            choice, g, bp, hc = zr.zr_choose_scheme(counts, n)
+            want_g = stats.gammas_from_counts(counts, nnz_total, n)
+            want_choice, want_bp, want_hc = stats.choose_scheme(want_g, n)
+            assert choice == want_choice
+            assert g == pytest.approx(want_g, rel=1e-12)
+            assert bp == pytest.approx(want_bp, rel=1e-12) and hc == pytest.approx(want_hc, rel=1e-12)
+    assert zr.zr_choose_scheme([10, 5], 3)[0] == -1     # not a power of two
+    assert zr.zr_choose_scheme([0, 0], 2)[0] == -1      # no entries
+    assert zr.zr_choose_scheme([10, -1], 2)[0] == -1
+
+
+def test_densification_argument_errors_before_launch(zr):
+    p = 1 << 40
+    ws = zr.zr_densification_workspace_size(4, 1000)
+    assert ws > 0
+    assert zr.zr_densification_workspace_size(3, 1000) == 0
+    call = lambda **kw: zr.zr_densification(  # noqa: E731
+        [p] * kw.get("n", 4), kw.get("nnz", [3, 4, 5, 6]), kw.get("n", 4), kw.get("m", 1000), p,
+        kw.get("ws", p), kw.get("ws_bytes", ws), None)
+    assert call(n=3, nnz=[1, 2, 3]) == zr.ZR_ERR_INVALID_ARG
+    assert call(m=0) == zr.ZR_ERR_INVALID_ARG
+    assert call(nnz=[3, -1, 5, 6]) == zr.ZR_ERR_INVALID_ARG
+    assert call(nnz=[3, 4, 5, 2000]) == zr.ZR_ERR_INVALID_ARG
+    assert call(ws=p + 8) == zr.ZR_ERR_ALIGNMENT
+    assert call(ws_bytes=ws - 1) == zr.ZR_ERR_CAPACITY
