@@ -77,6 +77,9 @@ def parse():
                     help="profiling: elements per rank of the dense component (default C2's)")
     ap.add_argument("--sparse", choices=("c4", "c5b"), default="c4",
                     help="profiling: sparse workload for --only sparse/partition")
+    ap.add_argument("--profile", choices=("c3", "sweep"), default=None,
+                    help="profiling: the C3 bf16 SkipReduce launches (p = 0, 1/4, 1/2), or the "
+                         "dense fp32 sweep N x M; prints one profiling line")
     return ap.parse_args()
 
 
@@ -435,11 +438,89 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------- main
+def time_launches(torch, fn, steps, warmup):
+    """Median CUDA-event time (ms) of ``fn`` over ``steps`` launches."""
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    times = []
+    for i in range(steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn(warmup + i)
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.median(times)
+
+
+def run_profile(args):
+    """C3 and the C5a sweep: one profiling line each (not the benchmark line).
+    Inputs are drawn on the device with torch's seeded generator (the parity
+    tests draw them on the host from the workload definitions)."""
+    import torch
+
+    import __graft_entry__
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    __graft_entry__.build()
+    import gradient_synchronisation_gb300 as zr
+
+    peak, _ = measured_hbm()
+    out = {"profiling": args.profile, "peak": peak, "steps": args.steps, "points": []}
+    if args.profile == "c3":
+        c = workloads.DENSE_C3
+        n, m = c["n"], c["m"]
+        g = torch.Generator(device=dev)
+        g.manual_seed(300)
+        x = (torch.randn((n, m), generator=g, device=dev) * c["sigma"]).to(torch.bfloat16)
+        bufs = [x[r] for r in range(n)]
+        for k in c["skip_ks"]:
+            ms = time_launches(torch, lambda i: zr.skipreduce(bufs, k=k, mode=zr.ZR_SKIP_RANDOM,
+                                                              seed=0, step=i),
+                               args.steps, args.warmup)
+            nbytes = (n - k) * m * 2 + n * m * 2
+            out["points"].append({"n": n, "m": m, "dtype": "bf16", "k": k, "bytes": nbytes,
+                                  "median_ms": ms, "gbs": nbytes / (ms / 1e3) / 1e9,
+                                  "frac": nbytes / (ms / 1e3) / 1e9 / peak})
+    else:
+        for n in workloads.SWEEP_NS:
+            for m in workloads.SWEEP_MS:
+                x = workloads.dense_device(n, m, 1e-3, 500 + n, dev)
+                bufs = [x[r] for r in range(n)]
+                # Captured in a CUDA graph and replayed, so that the time is
+                # the GPU's and not the host's launch path (which dominates at
+                # the small sizes).
+                reps = max(1, min(200, (1 << 26) // m))
+                zr.ring_allreduce(bufs, average=True)  # warm (and load) before capture
+                torch.cuda.synchronize()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph):
+                    for _ in range(reps):
+                        zr.ring_allreduce(bufs, average=True)
+                ms = time_launches(torch, lambda i: graph.replay(), args.steps, args.warmup) / reps
+                nbytes = 2 * n * m * 4
+                out["points"].append({"n": n, "m": m, "dtype": "f32", "bytes": nbytes,
+                                      "graph_reps": reps,
+                                      "median_ms": ms, "gbs": nbytes / (ms / 1e3) / 1e9,
+                                      "frac": nbytes / (ms / 1e3) / 1e9 / peak,
+                                      "l2_resident": nbytes < 129e6})
+                del x, bufs
+                torch.cuda.empty_cache()
+    print(json.dumps(out))
+    return 0
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.profile:
+        return run_profile(args)
 
     import torch
 

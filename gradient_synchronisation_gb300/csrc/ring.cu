@@ -65,8 +65,14 @@ struct BucketParams {
 };
 
 constexpr int kThreads = 128;
-constexpr int kBatch = 8;   // ranks whose loads are issued back to back before folding
-constexpr int kUnroll = 2;  // vectors per thread per pass
+// Default shape: kBatch ranks' loads issued back to back before folding,
+// kUnroll vectors per thread per pass.  Folds of at most 4 ranks take 4
+// vectors per thread (4 ranks per batch) instead, so that a thread still
+// keeps 256 bytes of loads in flight.
+constexpr int kBatch = 8;
+constexpr int kUnroll = 2;
+constexpr int kSmallBatch = 4;
+constexpr int kSmallUnroll = 4;
 
 template <typename T>
 struct Elem;
@@ -128,7 +134,7 @@ struct RingShared {
 
 // One block's share of slice c of job J: blocks bx = 0 .. J.bps - 1 cover
 // the slice's 16-byte vectors; block 0 also takes the scalar ends.
-template <typename T, bool kDrop>
+template <typename T, bool kDrop, int kUnroll, int kBatch>
 __device__ __forceinline__ void ring_slice(const void* const* bufs, const RingJob& J, int c, int bx,
                                            RingShared& S) {
   using E = Elem<T>;
@@ -225,11 +231,11 @@ __device__ __forceinline__ void ring_slice(const void* const* bufs, const RingJo
 }
 
 // One job: blockIdx.y is the slice, blockIdx.x the block inside it.
-template <typename T, bool kDrop>
+template <typename T, bool kDrop, int kU = kUnroll, int kB = kBatch>
 __global__ void __launch_bounds__(kThreads)
 ring_fused_kernel(const __grid_constant__ RingParams P) {
   __shared__ RingShared S;
-  ring_slice<T, kDrop>(P.bufs, P.job, blockIdx.y, blockIdx.x, S);
+  ring_slice<T, kDrop, kU, kB>(P.bufs, P.job, blockIdx.y, blockIdx.x, S);
 }
 
 // Many jobs (buckets) in one launch: block i belongs to the job whose block
@@ -247,7 +253,7 @@ ring_buckets_kernel(const __grid_constant__ BucketParams P) {
   }
   const RingJob& J = P.jobs[lo];
   const int local = i - P.block_start[lo];
-  ring_slice<T, false>(P.bufs, J, local / J.bps, local % J.bps, S);
+  ring_slice<T, false, kUnroll, kBatch>(P.bufs, J, local / J.bps, local % J.bps, S);
 }
 
 // Grid: blockIdx.y is the slice; blockIdx.x covers the slice's vectors with
@@ -256,10 +262,10 @@ ring_buckets_kernel(const __grid_constant__ BucketParams P) {
 // than a one-wave persistent grid (consecutive blocks sweep consecutive
 // addresses), and evict-first stores beat write-back stores by a wide margin.
 template <typename T>
-int blocks_per_slice(int64_t chunk) {
+int blocks_per_slice(int64_t chunk, int unroll = kUnroll) {
   constexpr int V = Elem<T>::kVec;
   const int64_t vecs_per_chunk = (chunk + V - 1) / V;
-  const int64_t per_block = (int64_t)kThreads * kUnroll;
+  const int64_t per_block = (int64_t)kThreads * unroll;
   int64_t gx = (vecs_per_chunk * 4 + per_block * 5 - 1) / (per_block * 5);
   if (gx > 0x7fffffff) gx = 0x7fffffff;
   if (gx < 1) gx = 1;
@@ -292,10 +298,16 @@ RingJob make_job(int n, int64_t m, int k, int mode, uint64_t seed, uint64_t step
 
 template <typename T>
 zr_status launch_one(RingParams& P, cudaStream_t stream) {
-  P.job.bps = blocks_per_slice<T>(P.job.chunk);
+  const bool small = P.job.n - P.job.k <= kSmallBatch;
+  P.job.bps = blocks_per_slice<T>(P.job.chunk, small ? kSmallUnroll : kUnroll);
   dim3 grid((unsigned)P.job.bps, (unsigned)P.job.n);
-  if (P.job.drop_thr != 0) ring_fused_kernel<T, true><<<grid, kThreads, 0, stream>>>(P);
-  else ring_fused_kernel<T, false><<<grid, kThreads, 0, stream>>>(P);
+  if (P.job.drop_thr != 0) {
+    if (small) ring_fused_kernel<T, true, kSmallUnroll, kSmallBatch><<<grid, kThreads, 0, stream>>>(P);
+    else ring_fused_kernel<T, true><<<grid, kThreads, 0, stream>>>(P);
+  } else {
+    if (small) ring_fused_kernel<T, false, kSmallUnroll, kSmallBatch><<<grid, kThreads, 0, stream>>>(P);
+    else ring_fused_kernel<T, false><<<grid, kThreads, 0, stream>>>(P);
+  }
   return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
 }
 
