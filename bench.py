@@ -56,8 +56,12 @@ TRAFFIC = {
 # Kernel launches each library call makes (counted from the library source).
 # Kernels of this library launched per component per step (the status-word
 # memset of the sparse path is a runtime memset, not counted).
-LAUNCHES = {"ring": 1, "skip": 1, "sparse": 5, "partition": 2, "dropout": 1, "buckets": 1,
-            "hb_encode": 3, "hb_decode": 4}
+LAUNCHES = {"ring": 1, "skip": 1, "sparse": 5, "partition": 3, "dropout": 1, "buckets": 1,
+            "hb_encode": 3, "hb_decode": 4, "hb_sets": 4}
+
+
+def torch_stream(torch):
+    return torch.cuda.current_stream().cuda_stream
 
 
 def parse():
@@ -69,7 +73,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only", choices=("ring", "skip", "sparse", "partition", "dropout", "buckets",
-                                       "hb_encode", "hb_decode"),
+                                       "hb_encode", "hb_decode", "hb_sets"),
                     default=None,
                     help="profiling: time one component alone (prints a profiling line, not the "
                          "benchmark line)")
@@ -203,7 +207,7 @@ class Workload:
         self.seed = c2["skip_seed"]
         self.dense_on = any(c in self.components for c in ("ring", "skip", "dropout", "buckets"))
         self.sparse_on = any(c in self.components
-                             for c in ("sparse", "partition", "hb_encode", "hb_decode"))
+                             for c in ("sparse", "partition", "hb_encode", "hb_decode", "hb_sets"))
         if self.dense_on:
             if dense_m:
                 self.host_dense = workloads.dense_f32_per_rank(self.n, self.m, c2["sigma"], 200)
@@ -243,7 +247,7 @@ class Workload:
                                 work=self.work)
             torch.cuda.synchronize()
             self.union = int(self.work.out_nnz.item())
-            if any(c in self.components for c in ("hb_encode", "hb_decode")):
+            if any(c in self.components for c in ("hb_encode", "hb_decode", "hb_sets")):
                 # Zen's Pull: every server's hash bitmap of the union's keys
                 self.hb = zr.HashBitmap(self.m4, self.parts, self.part_seed)
                 self.hb_keys = self.work.out_idx[:self.union]
@@ -251,6 +255,9 @@ class Workload:
                 self.hb_out = torch.empty(self.union, dtype=torch.int32, device=dev)
                 self.hb_koff = torch.empty(self.parts + 1, dtype=torch.int64, device=dev)
                 self.hb_bits = self.hb.bits.clone()
+                self.hb_sets_ws = torch.empty(
+                    zr.zr_partition_workspace_size(self.m4, self.parts), dtype=torch.uint8,
+                    device=dev)
 
     def bytes(self):
         s = 4
@@ -269,6 +276,8 @@ class Workload:
             out["hb_encode"] = self.m4 * 4 + self.union * 4 + words * 4
             # decode: the bitmaps, the index-set entries of the set bits, the keys out
             out["hb_decode"] = words * 4 + self.union * 4 * 2 + (self.parts + 1) * 8
+            # index sets: every index written once
+            out["hb_sets"] = self.m4 * 4 + (self.parts + 1) * 8
         return {c: out[c] for c in self.components}
 
     def run(self, name, i):
@@ -286,6 +295,10 @@ class Workload:
             self.hb.encode(self.hb_keys)
         elif name == "hb_decode":
             self.hb.decode(self.hb_bits, self.hb_out, self.hb_koff)
+        elif name == "hb_sets":
+            zr.zr_hash_index_sets(self.m4, self.parts, self.part_seed, self.hb.sets.data_ptr(),
+                                  self.hb.offsets.data_ptr(), self.hb_sets_ws.data_ptr(),
+                                  self.hb_sets_ws.numel(), torch_stream(self.torch))
         elif name == "sparse":
             zr.sparse_aggregate(self.d_idx, self.d_val, self.m4, self.parts, self.part_seed,
                                 work=self.work)

@@ -49,8 +49,8 @@ constexpr int kBatch = 8;                // entries per lane per load batch
 constexpr int kStartsUnroll = 4;         // starts kernel: groups of 4 keys per thread per step
 constexpr int kWriteWarps = 4;           // warps per CTA in the write kernel
 constexpr int kWriteThreads = kWriteWarps * 32;
-constexpr int kPartTile = 4096;          // zr_partition: entries per tile
-constexpr int kPartThreads = 512;
+constexpr int kPartTile = 1024;          // zr_partition: entries per tile
+constexpr int kPartThreads = 256;
 
 struct Lists {
   const int32_t* idx[ZR_MAX_RANKS];
@@ -76,70 +76,6 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-
-// ------------------------------------------------------------ positions
-// zr_partition: output positions come from per-tile entry counts per
-// partition, with two order-free sums kept beside them: the totals of every
-// segment of kSeg consecutive units and the grand total per partition, both
-// accumulated with integer atomics.  The first output position of unit u in
-// partition p is then
-//   sum_{p' < p} total[p'] + sum_{segments before u's} seg[.][p]
-//                          + sum_{units of u's segment before u} cnt[.][p],
-// which a CTA assembles with one round of parallel loads; no CTA ever waits
-// for another.
-constexpr int kSegLog = 6;
-constexpr int kSeg = 1 << kSegLog;
-
-__device__ void publish_counts(int64_t u, const int32_t* cnt, int parts, int32_t* cnt_g,
-                               unsigned long long* seg_g, unsigned long long* tot_g) {
-  for (int p = threadIdx.x; p < parts; p += blockDim.x) {
-    const int32_t c = cnt[p];
-    __stcg(cnt_g + u * parts + p, c);
-    if (c) {
-      atomicAdd(seg_g + (u >> kSegLog) * parts + p, (unsigned long long)c);
-      atomicAdd(tot_g + p, (unsigned long long)c);
-    }
-  }
-}
-
-// offs[0..parts] = exclusive prefix of the totals (shared memory); block 0
-// of the grid also writes it to d_offsets and the grand total to d_total.
-__device__ void partition_offsets(const unsigned long long* tot_g, int parts, long long* offs,
-                                  int64_t* d_offsets, int64_t* d_total) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    long long acc = 0;
-    for (int p = 0; p < parts; ++p) {
-      offs[p] = acc;
-      acc += (long long)__ldcg(tot_g + p);
-    }
-    offs[parts] = acc;
-    if (blockIdx.x == 0) {
-      if (d_offsets)
-        for (int p = 0; p <= parts; ++p) d_offsets[p] = offs[p];
-      if (d_total) *d_total = acc;
-    }
-  }
-  __syncthreads();
-}
-
-// base[p] = first output position of unit u in partition p (shared memory),
-// a warp per partition.  The caller puts a barrier after it.
-__device__ void unit_base(int64_t u, int parts, const long long* offs, const int32_t* cnt_g,
-                          const unsigned long long* seg_g, long long* base) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, warps = blockDim.x >> 5;
-  const int segs = (int)(u >> kSegLog);
-  const int64_t first = (int64_t)segs << kSegLog;
-  const int rest = (int)(u - first);
-  for (int p = warp; p < parts; p += warps) {
-    unsigned long long s = 0;
-    for (int j = lane; j < segs; j += 32) s += __ldcg(seg_g + (int64_t)j * parts + p);
-    for (int j = lane; j < rest; j += 32) s += (unsigned long long)__ldcg(cnt_g + (first + j) * parts + p);
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
-    if (lane == 0) base[p] = offs[p] + (long long)s;
-  }
-}
-
 
 // ------------------------------------------------------------ layout
 // Bins are W = 2^log_w keys: 1024, widened (up to 4096) only when the
@@ -768,18 +704,26 @@ bin_write_kernel(const __grid_constant__ Lists lists, int n, int log_w, int bins
 }
 
 // ------------------------------------------------------------ partition
-// [status | totals | segment totals] are contiguous so one memset clears them.
+// A stable split of one list by h0, tile by tile (kPartTile entries): a
+// count pass writes every tile's count per partition, the two scan kernels
+// of the union path turn them into each tile's first output position per
+// partition (and the partition totals), and a write pass places the tile's
+// entries.  No CTA waits for another and no counter is shared.
+// Workspace: [unused | totals | chunk totals | tile counts | tile prefixes]
+// (the partition path reports no device-side errors, so it has no status
+// word).
 struct PartLayout {
-  size_t tot, seg, cnt, total;
+  size_t tot, ctot, cnt, excl, total;
 };
 
 PartLayout part_layout(int64_t tiles, int parts) {
   PartLayout L;
-  const int64_t segs = (tiles + kSeg - 1) >> kSegLog;
+  const int64_t chunks = (tiles + kChunkBins - 1) >> kChunkLog;
   L.tot = 256;
-  L.seg = L.tot + align256((size_t)parts * 8);
-  L.cnt = L.seg + align256((size_t)segs * parts * 8);
-  L.total = L.cnt + align256((size_t)tiles * parts * 4);
+  L.ctot = L.tot + align256((size_t)parts * 8);
+  L.cnt = L.ctot + align256((size_t)chunks * parts * 8);
+  L.excl = L.cnt + align256((size_t)tiles * parts * 4);
+  L.total = L.excl + align256((size_t)tiles * parts * 8);
   return L;
 }
 
@@ -788,7 +732,7 @@ PartLayout part_layout(int64_t tiles, int parts) {
 template <bool kIdentity>
 __global__ void __launch_bounds__(kPartThreads)
 part_count_kernel(const int32_t* idx, int64_t nnz, int64_t tiles, H0 h, int parts,
-                  int32_t* cnt_g, unsigned long long* seg_g, unsigned long long* tot_g) {
+                  int32_t* cnt_g) {
   __shared__ int32_t cnt[ZR_MAX_PARTS];
   const int tid = threadIdx.x;
   const H0 hash = h;
@@ -803,7 +747,7 @@ part_count_kernel(const int32_t* idx, int64_t nnz, int64_t tiles, H0 h, int part
       if (live && (peers & lanemask_lt()) == 0) atomicAdd(&cnt[p], __popc(peers));
     }
     __syncthreads();
-    publish_counts(t, cnt, parts, cnt_g, seg_g, tot_g);
+    for (int q = tid; q < parts; q += kPartThreads) __stcg(cnt_g + (size_t)q * tiles + t, cnt[q]);
     __syncthreads();
   }
 }
@@ -813,21 +757,18 @@ part_count_kernel(const int32_t* idx, int64_t nnz, int64_t tiles, H0 h, int part
 template <bool kIdentity>
 __global__ void __launch_bounds__(kPartThreads)
 part_write_kernel(const int32_t* idx, const float* val, int64_t nnz, int64_t tiles, H0 h,
-                  int parts, const int32_t* cnt_g, const unsigned long long* seg_g,
-                  const unsigned long long* tot_g, int32_t* out_idx, float* out_val,
-                  int64_t* d_offsets) {
+                  int parts, const long long* excl_g, const long long* tot_g, int32_t* out_idx,
+                  float* out_val, int64_t* d_offsets) {
   extern __shared__ __align__(16) unsigned char smem[];
   long long* wbase = reinterpret_cast<long long*>(smem);  // warps * parts
   __shared__ long long offs[ZR_MAX_PARTS + 1];
-  __shared__ long long ubase[ZR_MAX_PARTS];
   constexpr int kPW = kPartThreads / 32;
   constexpr int kPerWarp = kPartTile / kPW;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const H0 hash = h;
-  partition_offsets(tot_g, parts, offs, d_offsets, nullptr);
+  load_partition_offsets(tot_g, parts, offs, d_offsets, nullptr);
   for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
     for (int q = threadIdx.x; q < kPW * parts; q += kPartThreads) wbase[q] = 0;
-    unit_base(t, parts, offs, cnt_g, seg_g, ubase);
     __syncthreads();
     const int64_t lo = t * kPartTile + (int64_t)warp * kPerWarp;
     const int64_t hi = min(t * kPartTile + kPartTile, nnz);
@@ -841,7 +782,7 @@ part_write_kernel(const int32_t* idx, const float* val, int64_t nnz, int64_t til
     }
     __syncthreads();
     for (int q = threadIdx.x; q < parts; q += kPartThreads) {
-      long long run = ubase[q];
+      long long run = offs[q] + __ldcg(excl_g + (size_t)q * tiles + t);
       for (int w = 0; w < kPW; ++w) {
         const long long c = wbase[w * parts + q];
         wbase[w * parts + q] = run;
@@ -1043,8 +984,9 @@ zr_status sparse_launch(const int32_t* const* idx, const float* const* val, cons
     bin_count_kernel<<<(unsigned)grid_for(warp_units, dinfo->count_per_sm), kBinThreads, 0,
                        stream>>>(lists, n, g.log_w, bins, starts, h, parts, cnt, status);
   }
-  bin_chunk_sum_kernel<<<dim3((unsigned)chunks, (unsigned)parts), kScanThreads, 0, stream>>>(
-      cnt, bins, ctot);
+  if (chunks > 1)  // with one chunk the scan needs no carry
+    bin_chunk_sum_kernel<<<dim3((unsigned)chunks, (unsigned)parts), kScanThreads, 0, stream>>>(
+        cnt, bins, ctot);
   bin_scan_kernel<<<dim3((unsigned)chunks, (unsigned)parts), kScanThreads, 0, stream>>>(
       cnt, ctot, bins, excl, tot);
   int64_t* offsets_out = n_parts > 0 ? d_offsets : nullptr;
@@ -1130,26 +1072,33 @@ zr_status partition_run(const int32_t* idx, const float* val, int64_t nnz, int n
   const int64_t tiles = (nnz + kPartTile - 1) / kPartTile;
   const PartLayout L = part_layout(tiles, n_parts);
   unsigned char* w = static_cast<unsigned char*>(ws);
-  unsigned long long* tot = reinterpret_cast<unsigned long long*>(w + L.tot);
-  unsigned long long* seg = reinterpret_cast<unsigned long long*>(w + L.seg);
+  long long* tot = reinterpret_cast<long long*>(w + L.tot);
+  long long* ctot = reinterpret_cast<long long*>(w + L.ctot);
   int32_t* cnt = reinterpret_cast<int32_t*>(w + L.cnt);
+  long long* excl = reinterpret_cast<long long*>(w + L.excl);
   const H0 h = make_h0(part_seed, (uint32_t)n_parts);
   if (tiles == 0) {
     if (cudaMemsetAsync(d_offsets, 0, (size_t)(n_parts + 1) * 8, stream) != cudaSuccess)
       return ZR_ERR_CUDA;
     return ZR_OK;
   }
+  if (tiles > 0x7fffffff) return ZR_ERR_UNSUPPORTED;
   DeviceInfo* dinfo = device_info();
   if (!dinfo) return ZR_ERR_CUDA;
-  if (cudaMemsetAsync(w, 0, L.cnt, stream) != cudaSuccess) return ZR_ERR_CUDA;
-  part_count_kernel<kIdentity><<<(unsigned)grid_for(tiles, dinfo->part_count_per_sm), kPartThreads, 0,
-                      stream>>>(idx, nnz, tiles, h, n_parts, cnt, seg, tot);
+  part_count_kernel<kIdentity><<<(unsigned)grid_for(tiles, dinfo->part_count_per_sm),
+                                 kPartThreads, 0, stream>>>(idx, nnz, tiles, h, n_parts, cnt);
+  const int chunks = (int)((tiles + kChunkBins - 1) >> kChunkLog);
+  // With one chunk the scan needs no carry, so the chunk sums are skipped.
+  if (chunks > 1)
+    bin_chunk_sum_kernel<<<dim3((unsigned)chunks, (unsigned)n_parts), kScanThreads, 0, stream>>>(
+        cnt, (int)tiles, ctot);
+  bin_scan_kernel<<<dim3((unsigned)chunks, (unsigned)n_parts), kScanThreads, 0, stream>>>(
+      cnt, ctot, (int)tiles, excl, tot);
   const size_t smem = (size_t)(kPartThreads / 32) * n_parts * sizeof(long long);
-  part_write_kernel<kIdentity><<<(unsigned)grid_for(tiles, 4), kPartThreads, smem, stream>>>(
-      idx, val, nnz, tiles, h, n_parts, cnt, seg, tot, out_idx, out_val, d_offsets);
+  part_write_kernel<kIdentity><<<(unsigned)grid_for(tiles, 8), kPartThreads, smem, stream>>>(
+      idx, val, nnz, tiles, h, n_parts, excl, tot, out_idx, out_val, d_offsets);
   return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
 }
-
 }  // namespace
 
 zr_status partition_launch(const int32_t* idx, const float* val, int64_t nnz, int n_parts,
