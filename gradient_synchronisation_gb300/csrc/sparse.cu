@@ -18,20 +18,23 @@
 //      and counts members per partition.
 //   3. scan:    one CTA per partition turns the per-bin counts into each
 //      bin's first output position in that partition.
-//   4. write:   per bin, a warp streams the bin's entries rank by rank in
-//      groups of up to 32 entries of one rank (the loads of several groups
-//      in flight at once) and folds them into a warp-private W-float window
-//      in ascending rank order: the first holder's value is stored, later
-//      holders are added, which is the left fold of the holders' values.
-//      Then each lane takes one bitmap word (32 keys in order), counts its
-//      members per partition, and after a prefix over lanes the
-//      members are written in ascending key order inside each partition.
+//   4. write:   per bin, a warp walks the bin rank by rank in chunks of up
+//      to 32 consecutive entries of one rank (the loads of 8 chunks in
+//      flight; one ballot gives each chunk's rank) and folds them into a
+//      warp-private W-float window in ascending rank order, which is the
+//      left fold of the holders' values.  Then the members are placed into
+//      their partitions' runs: through per-lane partition counters where
+//      bins hold few entries, partition by partition from per-partition
+//      member bitmaps where they hold many, and by a counting sort above 32
+//      partitions.  Each member's output position is its partition's offset
+//      plus the bin's prefix from step 3 plus its rank inside the bin, so
+//      members leave in ascending key order inside each partition.
 //
 // Every index taken from the inputs is range-checked before it addresses
 // shared memory, bounds read from the workspace are clamped to the list
-// lengths, and every output position is checked against the output
-// capacity, so malformed input can only produce wrong output and a status
-// word, never an out-of-bounds access.
+// lengths, and every output run (or position) is checked against the output
+// capacity before it is written, so malformed input can only produce wrong
+// output and a status word, never an out-of-bounds access.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -45,8 +48,8 @@ namespace {
 
 constexpr int kBinWarps = 8;             // warps per CTA in the count and write kernels
 constexpr int kBinThreads = kBinWarps * 32;
-constexpr int kBatch = 8;                // entries per lane per load batch
 constexpr int kStartsUnroll = 4;         // starts kernel: groups of 4 keys per thread per step
+constexpr int kBatch = 8;                // count pass: groups of 32 entries per load batch
 constexpr int kWriteWarps = 4;           // warps per CTA in the write kernel
 constexpr int kWriteThreads = kWriteWarps * 32;
 constexpr int kPartTile = 1024;          // zr_partition: entries per tile
@@ -208,12 +211,11 @@ bin_starts_kernel(const __grid_constant__ Lists lists, int dense_size, int log_w
   }
 }
 
-// Per-warp layout of one bin: rank r's entries are positions
-// [lo[r], lo[r] + len) of its list and [epre[r], epre[r+1]) of the bin's
-// rank-major flattened sequence.
-struct BinRanks {
-  int lo[ZR_MAX_RANKS];
-  int epre[ZR_MAX_RANKS + 1];
+// ------------------------------------------------------------ bin walk
+// A warp's view of one bin: lane r (and r + 32) holds rank r's first list
+// position in the bin (lo) and its entry count (len), clamped to the list.
+struct BinRows {
+  int lo[2], len[2];
 };
 
 // A bin's raw start rows for ranks lane and lane + 32, loaded ahead of use
@@ -237,6 +239,92 @@ __device__ __forceinline__ BinFetch bin_fetch(const int32_t* starts, int n, int 
   }
   return f;
 }
+
+__device__ __forceinline__ BinRows bin_rows(const Lists& lists, int n, const BinFetch& f) {
+  const int lane = threadIdx.x & 31;
+  BinRows R;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = lane + 32 * h;
+    int lo = 0, len = 0;
+    if (r < n) {
+      const int nnz = (int)lists.nnz[r];
+      lo = min(max(f.lo[h], 0), nnz);
+      len = min(max(f.hi[h], lo), nnz) - lo;
+    }
+    R.lo[h] = lo;
+    R.len[h] = len;
+  }
+  return R;
+}
+
+// Rank r's value (r < 64, the same on every lane) from the lane holding it.
+__device__ __forceinline__ int rank_get(const int (&v)[2], int r) {
+  return __shfl_sync(0xffffffffu, (r & 32) ? v[1] : v[0], r & 31);
+}
+
+// Walks the bin rank by rank, lowest rank first, in chunks of up to 32
+// consecutive entries of one rank: lane l takes entry 32c + l of chunk c of
+// its rank.  The loads of kChunks chunks are issued together (load(t, rank,
+// pos) fills slot t), then apply(t, ok) runs for the chunks in order, ok
+// saying whether the lane holds an entry.  A list is strictly ascending, so
+// the keys of one chunk are distinct and a chunk is applied at once; chunks
+// go in rank order, so a key held by several ranks meets the lowest rank
+// first.  Rank r's chunks are numbers [cp_r, cp_r + nc_r) of the bin; the
+// rank of chunk j is the number of ranks whose chunks end at or before j,
+// one ballot, so the walk has no data-dependent branch.
+template <int kChunks, typename Load, typename Apply>
+__device__ __forceinline__ void walk_bin(const BinRows& R, int n, Load&& load, Apply&& apply) {
+  const int lane = threadIdx.x & 31;
+  int cp[2], cend[2];
+  int carry = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int nc = (R.len[h] + 31) >> 5;
+    const int incl = warp_incl_scan(nc);
+    cp[h] = carry + incl - nc;
+    cend[h] = carry + incl;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  const int chunks = carry;
+  const bool live0 = lane < n, live1 = lane + 32 < n;
+  for (int j0 = 0; j0 < chunks; j0 += kChunks) {
+    bool ok[kChunks];
+#pragma unroll
+    for (int t = 0; t < kChunks; ++t) {
+      const int j = j0 + t;
+      ok[t] = false;
+      if (j < chunks) {
+        int r = __popc(__ballot_sync(0xffffffffu, live0 && cend[0] <= j));
+        if (n > 32) r += __popc(__ballot_sync(0xffffffffu, live1 && cend[1] <= j));
+        // every lane takes part in the shuffles, then the lanes past the
+        // rank's end load nothing
+        const int i = ((j - rank_get(cp, r)) << 5) + lane;
+        const int len = rank_get(R.len, r);
+        const int lo = rank_get(R.lo, r);
+        if (i < len) {
+          ok[t] = true;
+          load(t, r, lo + i);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kChunks; ++t) {
+      if (j0 + t < chunks) {
+        apply(t, ok[t]);
+        __syncwarp();
+      }
+    }
+  }
+}
+
+// The count pass walks a bin flattened: rank r's entries are positions
+// [lo[r], lo[r] + len) of its list and [epre[r], epre[r+1]) of the bin's
+// rank-major flattened sequence.
+struct BinRanks {
+  int lo[ZR_MAX_RANKS];
+  int epre[ZR_MAX_RANKS + 1];
+};
 
 // Clamps the fetched rows to the list lengths and fills R (warp-collective;
 // ends with __syncwarp).  Returns the bin's entry count.
@@ -479,219 +567,359 @@ __device__ void load_partition_offsets(const long long* tot_g, int parts, long l
   __syncthreads();
 }
 
-// Warp-private shared memory of the writer: acc[W] (f32, first, so that it
-// is 16-byte aligned), wdelta[parts] (i64), ub[W/32], run[parts] (i32),
-// mlist[W] and stage[W] (u16).
+// How the writer places a bin's members into their partitions' runs:
+//   kPlaceLane  per-lane partition counters (at most 32 partitions; bins with
+//               few members, where a pass per partition would mostly idle);
+//   kPlaceMask  per-partition member bitmaps, emitted partition by partition
+//               (at most 32 partitions; bins with many members);
+//   kPlaceSort  a counting sort of the bin's member list (any partition count).
+enum Placement { kPlaceLane = 0, kPlaceMask = 1, kPlaceSort = 2 };
+
+// Warp-private shared memory of the writer; acc[W] (f32) comes first, so
+// that it is 16-byte aligned, then ub[W/32] and
+//   kPlaceLane: the lanes' partition counters (32 rows of row_words(parts)
+//               words, two 16-bit counters per word) and the bin's run
+//               bases gbs[parts] (i64);
+//   kPlaceMask: the member bitmaps pm[parts][W/32];
+//   kPlaceSort: run[parts] (i32), wdelta[parts] (i64), mlist[W] and
+//               stage[W] (u16).
+__host__ __device__ inline int row_words(int parts) {
+  return ((parts + 1) >> 1) | 1;  // odd, so lane rows fall in distinct banks
+}
+
+template <int kPlace>
 __host__ __device__ inline size_t warp_smem_bytes(int log_w, int parts) {
-  const size_t W = (size_t)1 << log_w;
-  const size_t b = (size_t)parts * 8 + W * 4 + (W / 32) * 4 + (size_t)parts * 4 + W * 2 + W * 2;
+  const size_t W = (size_t)1 << log_w, words = W / 32, P = (size_t)parts;
+  size_t b = W * 4 + words * 4;
+  if (kPlace == kPlaceLane) b += 32 * 4 * (size_t)row_words(parts) + P * 8;
+  else if (kPlace == kPlaceMask) b += words * 4 * P;
+  else b += ((P + 1) & ~(size_t)1) * 4 + P * 8 + W * 4;
   return (b + 15) & ~(size_t)15;
 }
 
+// The 1/N average: none, a multiply by the exact reciprocal (N a power of
+// two, where it equals the correctly rounded quotient), or the correctly
+// rounded division.
+enum AvgKind { kAvgNone = 0, kAvgPow2 = 1, kAvgDiv = 2 };
+
+template <int kAvg>
+__device__ __forceinline__ float averaged(float v, float fn, float inv) {
+  if (kAvg == kAvgPow2) return v * inv;
+  if (kAvg == kAvgDiv) return __fdiv_rn(v, fn);
+  return v;
+}
+
+constexpr int kWriteChunks = 8;
+// Average entries per 1024-key bin from which the writer emits partition by
+// partition (kPlaceMask): measured on the C4 embedding lists (82 entries a
+// bin, per-lane counters faster) and the C5b top-k lists (819 a bin, the
+// bitmaps faster).
+constexpr int64_t kMaskMinPerBin = 256;
+
 // Per bin:
-//   fold    entries in flattened rank-major order into acc[]; inside a group
-//           of 32 the lanes are applied one rank at a time, lowest first, so
-//           every member is the left fold of its holders in rank order (the
-//           bitmap's old bit says whether a slot already holds a value);
-//   list    the members' slots in ascending key order (mlist);
-//   place   a counting sort of mlist by partition into stage[], stable, so
-//           stage[] is the bin's output in partition-major, ascending-key
-//           order (run[p] starts at the bin-local prefix of the counts);
-//   emit    stage[] 32 entries at a time; entry j of partition p goes to
-//           offs[p] + excl[p][b] + (j - pstart[p]), so each partition's run
-//           of the bin leaves as one contiguous, coalesced store.
+//   fold    the bin's entries rank by rank (walk_bin) into acc[], which
+//           starts at -0.0, the identity of the fold (-0.0 + x == x for
+//           every x that is not a NaN), so every member ends as the left fold
+//           of its holders in rank order; the union bitmap ub is ORed alongside.
+//   kPlaceLane:
+//     count lane l takes the ub words of keys [32 wpl l, 32 wpl (l + 1)) (its
+//           members, in key order), hashes each member and counts it in its
+//           own row of 16-bit counters, one per partition, two per word;
+//     scan  a prefix over the lanes of each counter word (two partitions at
+//           once) turns the rows into each lane's first position inside the
+//           bin's run of every partition; the totals are checked against the
+//           count pass and the output bounds;
+//     emit  each lane walks its members again in key order and writes each
+//           to gbs[p] + its counter, then advances the counter.
+//   kPlaceMask:
+//     mask  lane l takes ub words l, l + 32, ...: each member is hashed and
+//           its bit set in pm[p] (a lane owns its words, so no two lanes
+//           write one word);
+//     emit  partition by partition, lane l takes pm[p] words l, l + 32, ...;
+//           a prefix of their popcounts over the lanes gives each lane the
+//           position of its first member inside the bin's run of p, and the
+//           lane writes its members in ascending key order;
+//   kPlaceSort:
+//     list  the members' slots in ascending key order (mlist);
+//     place a stable counting sort of mlist by partition into stage[]
+//           (match_any groups the lanes of one partition);
+//     emit  stage[] 32 entries at a time to offs[p] + excl[p][b] + its rank
+//           inside the bin's run of partition p.
+// ub, the counters and pm are cleared after use; acc is reset per bin.
+template <int kPlace, int kAvg>
 __global__ void __launch_bounds__(kWriteThreads)
 bin_write_kernel(const __grid_constant__ Lists lists, int n, int log_w, int bins,
-                 const int32_t* starts, H0 h, int parts, int average, const int32_t* cnt_g,
+                 const int32_t* starts, H0 h, int parts, const int32_t* cnt_g,
                  const long long* excl_g, const long long* tot_g, int32_t* out_idx,
                  float* out_val, int64_t out_cap, int64_t* d_offsets, int64_t* d_total,
                  int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ long long offs[ZR_MAX_PARTS + 1];
-  __shared__ BinRanks ranks_all[kWriteWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  BinRanks& R = ranks_all[warp];
   const int W = 1 << log_w;
-  const int words = W >> 5, wpl = words >> 5;
-  unsigned char* mine = smem + (size_t)warp * warp_smem_bytes(log_w, parts);
+  const int words = W >> 5;
+  constexpr bool kLane = kPlace == kPlaceLane;
+  constexpr bool kMask = kPlace == kPlaceMask;
+  unsigned char* mine = smem + (size_t)warp * warp_smem_bytes<kPlace>(log_w, parts);
   float* acc = reinterpret_cast<float*>(mine);
-  long long* wdelta = reinterpret_cast<long long*>(acc + W);
-  uint32_t* ub = reinterpret_cast<uint32_t*>(wdelta + parts);
-  int32_t* run = reinterpret_cast<int32_t*>(ub + words);
-  uint16_t* mlist = reinterpret_cast<uint16_t*>(run + parts);
-  uint16_t* stage = mlist + W;
   const H0 hash = h;
-  const float fn = (float)n;
+  const float fn = (float)n, inv = 1.0f / (float)n;
   const unsigned lt = lanemask_lt();
   load_partition_offsets(tot_g, parts, offs, d_offsets, d_total);
 
+  const int wpl = words >> 5;  // bitmap words per lane
+  const int rs = row_words(parts);
+  uint32_t* ub = reinterpret_cast<uint32_t*>(acc + W);
+  uint32_t* rows = nullptr;
+  long long* gbs = nullptr;
+  uint32_t* pm = nullptr;
+  long long* wdelta = nullptr;
+  int32_t* run = nullptr;
+  uint16_t* mlist = nullptr;
+  uint16_t* stage = nullptr;
+  if (kLane) {
+    rows = ub + words;
+    gbs = reinterpret_cast<long long*>(rows + 32 * rs);
+    for (int i = lane; i < words + 32 * rs; i += 32) ub[i] = 0;  // ub and the rows
+  } else if (kMask) {
+    pm = ub + words;
+    for (int i = lane; i < words * (parts + 1); i += 32) ub[i] = 0;  // ub and pm
+  } else {
+    run = reinterpret_cast<int32_t*>(ub + words);
+    wdelta = reinterpret_cast<long long*>(run + ((parts + 1) & ~1));
+    mlist = reinterpret_cast<uint16_t*>(wdelta + parts);
+    stage = mlist + W;
+    for (int i = lane; i < words; i += 32) ub[i] = 0;
+  }
+  __syncwarp();
+
   const int nwarps = gridDim.x * kWriteWarps;
   int b = blockIdx.x * kWriteWarps + warp;
+  // next bin's start rows, and (kLane, kMask) lane p's count and prefix for it
   BinFetch fetch = {};
-  if (b < bins) fetch = bin_fetch(starts, n, bins, b);
+  int pc_next = 0;
+  long long pe_next = 0;
+  if (b < bins) {
+    fetch = bin_fetch(starts, n, bins, b);
+    if ((kLane || kMask) && lane < parts) {
+      pc_next = __ldcg(cnt_g + (size_t)lane * bins + b);
+      pe_next = __ldcg(excl_g + (size_t)lane * bins + b);
+    }
+  }
   for (; b < bins; b += nwarps) {
     const uint32_t base = (uint32_t)b << log_w;
-    for (int w = lane; w < words; w += 32) ub[w] = 0;
-    // -0.0 is the identity of the fold: -0.0 + x == x for every x that is
-    // not a NaN, so each member ends as the left fold of its holders.
+    const BinRows R = bin_rows(lists, n, fetch);
+    const int pc = pc_next;
+    const long long pe = pe_next;
+    if (b + nwarps < bins) {
+      fetch = bin_fetch(starts, n, bins, b + nwarps);
+      if ((kLane || kMask) && lane < parts) {
+        pc_next = __ldcg(cnt_g + (size_t)lane * bins + b + nwarps);
+        pe_next = __ldcg(excl_g + (size_t)lane * bins + b + nwarps);
+      }
+    }
     for (int i = lane; i < (W >> 2); i += 32)
       reinterpret_cast<float4*>(acc)[i] = make_float4(-0.0f, -0.0f, -0.0f, -0.0f);
-    // This bin's partition runs: pstart[p] (bin-local) and the global base.
-    int expect = 0, run0 = 0;
-    for (int p0 = 0; p0 < parts; p0 += 32) {
-      const int p = p0 + lane;
-      const int c = p < parts ? __ldcg(cnt_g + (size_t)p * bins + b) : 0;
-      const long long e = p < parts ? __ldcg(excl_g + (size_t)p * bins + b) : 0;
-      const int incl = warp_incl_scan(c);
-      if (p0 == 0) run0 = incl - c;
-      if (p < parts) {
-        run[p] = expect + incl - c;
-        wdelta[p] = offs[p] + e - (expect + incl - c);
-      }
-      expect += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    const int total = bin_commit(lists, n, fetch, R);
-    if (b + nwarps < bins) fetch = bin_fetch(starts, n, bins, b + nwarps);
+    __syncwarp();
 
-    int key[kBatch];
-    float val[kBatch];
-    for_bin_entries(
-        lists, n, R, total, status,
+    // fold
+    int key[kWriteChunks];
+    float val[kWriteChunks];
+    walk_bin<kWriteChunks>(
+        R, n,
         [&](int t, int r, int pos) {
           key[t] = __ldg(lists.idx[r] + pos);
           val[t] = __ldg(lists.val[r] + pos);
         },
-        [&](int k0, const int (&rank)[kBatch]) {
-          // Group by group.  Keys that strictly ascend across the lanes of
-          // a group are all distinct, so such a group is applied at once;
-          // otherwise each maximal ascending run of lanes is applied in
-          // lane order (ranks never decrease along the lanes, so a key held
-          // by two ranks meets the lower rank first).
-#pragma unroll
-          for (int t = 0; t < kBatch; ++t) {
-            if (k0 + 32 * t < total) {
-              const uint32_t slot = (uint32_t)key[t] - base;
-              const bool live = rank[t] >= 0;
-              const bool in = live && slot < (uint32_t)W;
-              const int prev = __shfl_up_sync(0xffffffffu, key[t], 1);
-              const unsigned desc = __ballot_sync(0xffffffffu, live && lane > 0 && prev >= key[t]);
-              if (desc == 0) {
-                if (in) {
-                  acc[slot] = __fadd_rn(acc[slot], val[t]);
-                  atomicOr(&ub[slot >> 5], 1u << (slot & 31));
-                }
-              } else {
-                const int run_id = __popc(desc & (lt | (1u << lane)));
-                const int runs = __popc(desc) + 1;
-                for (int q = 0; q < runs; ++q) {
-                  if (in && run_id == q) {
-                    acc[slot] = __fadd_rn(acc[slot], val[t]);
-                    atomicOr(&ub[slot >> 5], 1u << (slot & 31));
-                  }
-                  __syncwarp();
-                }
-              }
-              __syncwarp();
-            }
+        [&](int t, bool ok) {
+          const uint32_t slot = (uint32_t)key[t] - base;
+          if (ok && slot < (uint32_t)W) {
+            acc[slot] = __fadd_rn(acc[slot], val[t]);
+            atomicOr(&ub[slot >> 5], 1u << (slot & 31));
           }
         });
-    __syncwarp();
+
+    if (kLane) {
+      uint32_t* row = rows + lane * rs;
+      uint16_t* row16 = reinterpret_cast<uint16_t*>(row);
+      // count
+      for (int q = 0; q < wpl; ++q) {
+        const int w = lane * wpl + q;
+        uint32_t bits = ub[w];
+        while (bits) {
+          const int bit = __ffs(bits) - 1;
+          bits &= bits - 1;
+          const int p = parts > 1 ? (int)hash(base + (uint32_t)(w * 32 + bit)) : 0;
+          if ((unsigned)p < (unsigned)parts) row16[p] = (uint16_t)(row16[p] + 1);
+          else flag(status, ZR_ERR_INTERNAL);
+        }
+      }
+      // scan (every field stays below 2^16: a bin has at most 4096 members)
+      int mytot = 0;
+      for (int q = 0; q < (parts + 1) >> 1; ++q) {
+        const uint32_t v = row[q];
+        const uint32_t incl = (uint32_t)warp_incl_scan((int)v);
+        row[q] = incl - v;
+        const uint32_t tq = __shfl_sync(0xffffffffu, incl, 31);
+        if ((lane >> 1) == q) mytot = (int)((lane & 1) ? tq >> 16 : tq & 0xffffu);
+      }
+      // The count pass saw the same entries, so every run has the counted
+      // size and lies inside the output; a bin where one does not is not
+      // written.
+      bool bad = false;
+      if (lane < parts) {
+        const long long g = offs[lane] + pe;
+        bad = mytot != pc || g < 0 || g + pc > out_cap;
+        gbs[lane] = g;
+      }
+      const bool skip = __any_sync(0xffffffffu, bad);
+      if (skip && lane == 0) flag(status, ZR_ERR_INTERNAL);
+      __syncwarp();
+      // emit
+      for (int q = 0; q < wpl; ++q) {
+        const int w = lane * wpl + q;
+        uint32_t bits = skip ? 0u : ub[w];
+        ub[w] = 0;
+        while (bits) {
+          const int bit = __ffs(bits) - 1;
+          bits &= bits - 1;
+          const int slot = w * 32 + bit;
+          const int p = parts > 1 ? (int)hash(base + (uint32_t)slot) : 0;
+          if ((unsigned)p < (unsigned)parts) {
+            const int at = row16[p];
+            row16[p] = (uint16_t)(at + 1);
+            const long long dst = gbs[p] + at;
+            out_idx[dst] = (int32_t)(base + (uint32_t)slot);
+            out_val[dst] = averaged<kAvg>(acc[slot], fn, inv);
+          }
+        }
+      }
+      for (int q = 0; q < rs; ++q) row[q] = 0;
+      __syncwarp();
+      continue;
+    }
+
+    if (kMask) {
+      // mask
+      for (int w = lane; w < words; w += 32) {
+        uint32_t bits = ub[w];
+        ub[w] = 0;
+        while (bits) {
+          const int bit = __ffs(bits) - 1;
+          bits &= bits - 1;
+          const int p = parts > 1 ? (int)hash(base + (uint32_t)(w * 32 + bit)) : 0;
+          if ((unsigned)p < (unsigned)parts) pm[p * words + w] |= 1u << bit;
+          else flag(status, ZR_ERR_INTERNAL);
+        }
+      }
+      __syncwarp();
+      // emit
+      const long long gb = lane < parts ? offs[lane] + pe : 0;
+      for (int p = 0; p < parts; ++p) {
+        const long long g = __shfl_sync(0xffffffffu, gb, p);
+        const int want = __shfl_sync(0xffffffffu, pc, p);
+        // The count pass saw the same entries, so the run has want members
+        // and lies inside the output; a run that does not is not written.
+        const bool fits = g >= 0 && g + want <= out_cap;
+        int32_t* oi = out_idx + (fits ? g : 0);
+        float* ov = out_val + (fits ? g : 0);
+        uint32_t* pmp = pm + p * words;
+        int carry = 0;
+        for (int w0 = 0; w0 < words; w0 += 32) {
+          const int w = w0 + lane;
+          uint32_t bits = 0;
+          if (w < words) {
+            bits = pmp[w];
+            pmp[w] = 0;
+          }
+          const int c = __popc(bits);
+          const int incl = warp_incl_scan(c);
+          int at = carry + incl - c;
+          carry += __shfl_sync(0xffffffffu, incl, 31);
+          if (!fits || carry > want) continue;
+          while (bits) {
+            const int bit = __ffs(bits) - 1;
+            bits &= bits - 1;
+            const int slot = w * 32 + bit;
+            oi[at] = (int32_t)(base + (uint32_t)slot);
+            ov[at] = averaged<kAvg>(acc[slot], fn, inv);
+            ++at;
+          }
+        }
+        if (lane == 0 && (!fits || carry != want))
+          flag(status, fits ? ZR_ERR_INTERNAL : ZR_ERR_INPUT_UNSORTED);
+      }
+      __syncwarp();
+      continue;
+    }
 
     // list: lane l owns words [l * wpl, (l + 1) * wpl)
     int mine_cnt = 0;
     for (int q = 0; q < wpl; ++q) mine_cnt += __popc(ub[lane * wpl + q]);
     const int incl = warp_incl_scan(mine_cnt);
     const int members = __shfl_sync(0xffffffffu, incl, 31);
-    if (members != expect) {
-      // The count pass saw the same entries, so this cannot happen.
-      if (lane == 0) flag(status, ZR_ERR_INTERNAL);
-      __syncwarp();
-      continue;
-    }
     int at = incl - mine_cnt;
     for (int q = 0; q < wpl; ++q) {
       const int w = lane * wpl + q;
       uint32_t bits = ub[w];
+      ub[w] = 0;
       while (bits) {
         const int bit = __ffs(bits) - 1;
         bits &= bits - 1;
         mlist[at++] = (uint16_t)(w * 32 + bit);
       }
     }
-    __syncwarp();
-
-    // place
-    if (parts <= 32) {
-      // Lane q keeps partition q's next stage position.  Per step of 32
-      // members, nbits ballots of the partition bits give every lane the
-      // set of lanes that share its partition (its rank among them) and
-      // lane q the number of members in partition q.
-      const int nbits = parts > 1 ? 32 - __clz(parts - 1) : 0;
-      int runq = run0;
-      for (int j0 = 0; j0 < members; j0 += 32) {
-        const int j = j0 + lane;
-        bool live = j < members;
-        const int slot = live ? mlist[j] : 0;
-        int p = parts > 1 ? (int)hash(base + (uint32_t)slot) : 0;
-        if (live && (unsigned)p >= (unsigned)parts) {
-          flag(status, ZR_ERR_INTERNAL);
-          live = false;
-        }
-        if (!live) p = 0;
-        const unsigned all = __ballot_sync(0xffffffffu, live);
-        unsigned same = all, mine_q = all;
-#pragma unroll
-        for (int i = 0; i < 5; ++i) {
-          if (i < nbits) {
-            const unsigned bi = __ballot_sync(0xffffffffu, (p >> i) & 1);
-            same &= ((p >> i) & 1) ? bi : ~bi;
-            mine_q &= ((lane >> i) & 1) ? bi : ~bi;
-          }
-        }
-        const int at_p = __shfl_sync(0xffffffffu, runq, p);
-        if (live) {
-          const int sidx = at_p + __popc(same & lt);
-          if ((unsigned)sidx < (unsigned)members) stage[sidx] = (uint16_t)slot;
-          else flag(status, ZR_ERR_INTERNAL);
-        }
-        runq += __popc(mine_q);
+    // This bin's partition runs: run[p] (bin-local start) and the global base.
+    int expect = 0;
+    for (int p0 = 0; p0 < parts; p0 += 32) {
+      const int p = p0 + lane;
+      const int c = p < parts ? __ldcg(cnt_g + (size_t)p * bins + b) : 0;
+      const long long e = p < parts ? __ldcg(excl_g + (size_t)p * bins + b) : 0;
+      const int pincl = warp_incl_scan(c);
+      if (p < parts) {
+        run[p] = expect + pincl - c;
+        wdelta[p] = offs[p] + e - (expect + pincl - c);
       }
-    } else {
-      for (int j0 = 0; j0 < members; j0 += 32) {
-        const int j = j0 + lane;
-        const bool live = j < members;
-        const int slot = live ? mlist[j] : 0;
-        int p = live ? (int)hash(base + (uint32_t)slot) : parts;
-        if (live && (unsigned)p >= (unsigned)parts) {
-          flag(status, ZR_ERR_INTERNAL);
-          p = parts;
-        }
-        const bool ok = live && p < parts;
-        const unsigned peers = __match_any_sync(0xffffffffu, p);
-        if (ok) {
-          const int sidx = run[p] + __popc(peers & lt);
-          if ((unsigned)sidx < (unsigned)members) stage[sidx] = (uint16_t)slot;
-          else flag(status, ZR_ERR_INTERNAL);
-        }
-        __syncwarp();
-        if (ok && (peers & lt) == 0) run[p] += __popc(peers);
-        __syncwarp();
-      }
+      expect += __shfl_sync(0xffffffffu, pincl, 31);
     }
     __syncwarp();
-
+    if (members != expect) {
+      // The count pass saw the same entries, so this cannot happen.
+      if (lane == 0) flag(status, ZR_ERR_INTERNAL);
+      __syncwarp();
+      continue;
+    }
+    // place
+    for (int j0 = 0; j0 < members; j0 += 32) {
+      const int j = j0 + lane;
+      const bool live = j < members;
+      const int slot = live ? mlist[j] : 0;
+      int p = live ? (int)hash(base + (uint32_t)slot) : parts;
+      if (live && (unsigned)p >= (unsigned)parts) {
+        flag(status, ZR_ERR_INTERNAL);
+        p = parts;
+      }
+      const bool ok = live && p < parts;
+      const unsigned peers = __match_any_sync(0xffffffffu, p);
+      if (ok) {
+        const int sidx = run[p] + __popc(peers & lt);
+        if ((unsigned)sidx < (unsigned)members) stage[sidx] = (uint16_t)slot;
+        else flag(status, ZR_ERR_INTERNAL);
+      }
+      __syncwarp();
+      if (ok && (peers & lt) == 0) run[p] += __popc(peers);
+      __syncwarp();
+    }
     // emit
     for (int j = lane; j < members; j += 32) {
       const int slot = stage[j];
       const uint32_t k = base + (uint32_t)slot;
-      const int p = parts > 1 ? (int)hash(k) : 0;
+      const int p = (int)hash(k);
       if (slot < W && (unsigned)p < (unsigned)parts) {
         const long long dst = wdelta[p] + j;
-        float v = acc[slot];
-        if (average) v = __fdiv_rn(v, fn);
         if (dst >= 0 && dst < out_cap) {
           out_idx[dst] = (int32_t)k;
-          out_val[dst] = v;
+          out_val[dst] = averaged<kAvg>(acc[slot], fn, inv);
         } else {
           flag(status, ZR_ERR_INPUT_UNSORTED);
         }
@@ -903,6 +1131,28 @@ int64_t grid_for(int64_t units, int blocks_per_sm) {
   return g < 1 ? 1 : g;
 }
 
+// The write kernel for a placement (partition masks or the sort) and an
+// average mode.
+template <int kPlace>
+const void* write_kernel_avg(int avg_kind) {
+  if (avg_kind == kAvgPow2) return (const void*)bin_write_kernel<kPlace, kAvgPow2>;
+  if (avg_kind == kAvgDiv) return (const void*)bin_write_kernel<kPlace, kAvgDiv>;
+  return (const void*)bin_write_kernel<kPlace, kAvgNone>;
+}
+
+const void* write_kernel(int place, int avg_kind) {
+  if (place == kPlaceLane) return write_kernel_avg<kPlaceLane>(avg_kind);
+  if (place == kPlaceMask) return write_kernel_avg<kPlaceMask>(avg_kind);
+  return write_kernel_avg<kPlaceSort>(avg_kind);
+}
+
+size_t write_smem(int place, int log_w, int parts) {
+  const size_t per_warp = place == kPlaceLane   ? warp_smem_bytes<kPlaceLane>(log_w, parts)
+                          : place == kPlaceMask ? warp_smem_bytes<kPlaceMask>(log_w, parts)
+                                                : warp_smem_bytes<kPlaceSort>(log_w, parts);
+  return kWriteWarps * per_warp;
+}
+
 // Per-device cached occupancy, and the dynamic shared-memory opt-in of the
 // write kernels (done once per device).
 struct DeviceInfo {
@@ -917,10 +1167,14 @@ DeviceInfo* device_info() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   DeviceInfo& d = info[dev];
   if (!d.ready) {
-    const int write_max = (int)(kWriteWarps * warp_smem_bytes(12, ZR_MAX_PARTS));
-    if (cudaFuncSetAttribute(bin_write_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             write_max) != cudaSuccess)
-      return nullptr;
+    for (int place = 0; place < 3; ++place) {
+      const int most = (int)write_smem(place, 12, place == kPlaceSort ? ZR_MAX_PARTS : 32);
+      for (int a = 0; a < 3; ++a)
+        if (cudaFuncSetAttribute(write_kernel(place, a),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 most) != cudaSuccess)
+          return nullptr;
+    }
     d.count_per_sm = per_sm((const void*)bin_count_kernel, kBinThreads, 0);
     d.part_count_per_sm = per_sm((const void*)part_count_kernel<false>, kPartThreads, 0);
     d.ready = 1;
@@ -990,12 +1244,26 @@ zr_status sparse_launch(const int32_t* const* idx, const float* const* val, cons
   bin_scan_kernel<<<dim3((unsigned)chunks, (unsigned)parts), kScanThreads, 0, stream>>>(
       cnt, ctot, bins, excl, tot);
   int64_t* offsets_out = n_parts > 0 ? d_offsets : nullptr;
-  const size_t smem = kWriteWarps * warp_smem_bytes(g.log_w, parts);
-  const int o = per_sm((const void*)bin_write_kernel, kWriteThreads, smem);
+  const int avg_kind = !average ? kAvgNone : ((n & (n - 1)) == 0 ? kAvgPow2 : kAvgDiv);
   const int64_t write_units = (g.bins + kWriteWarps - 1) / kWriteWarps;
-  bin_write_kernel<<<(unsigned)grid_for(write_units, o), kWriteThreads, smem, stream>>>(
-      lists, n, g.log_w, bins, starts, h, parts, average, cnt, excl, tot, out_idx, out_val,
-      out_cap, offsets_out, d_out_nnz, status);
+  // Bins with many members (on average) are emitted partition by partition,
+  // others through per-lane counters; more than 32 partitions take the sort.
+  const int place = parts > 32                                        ? kPlaceSort
+                    : g.log_w == 10 && total_nnz >= kMaskMinPerBin * g.bins ? kPlaceMask
+                                                                        : kPlaceLane;
+  const size_t smem = write_smem(place, g.log_w, parts);
+  const void* fn = write_kernel(place, avg_kind);
+  const int o = per_sm(fn, kWriteThreads, smem);
+  const unsigned grid = (unsigned)grid_for(write_units, o);
+  const int32_t* cnt_c = cnt;
+  const long long* excl_c = excl;
+  const long long* tot_c = tot;
+  void* args[] = {(void*)&lists, (void*)&n, (void*)&g.log_w, (void*)&bins, (void*)&starts,
+                  (void*)&h, (void*)&parts, (void*)&cnt_c, (void*)&excl_c, (void*)&tot_c,
+                  (void*)&out_idx, (void*)&out_val, (void*)&out_cap, (void*)&offsets_out,
+                  (void*)&d_out_nnz, (void*)&status};
+  if (cudaLaunchKernel(fn, dim3(grid), dim3(kWriteThreads), args, smem, stream) != cudaSuccess)
+    return ZR_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
 }
 

@@ -106,6 +106,38 @@ def test_wide_key_range_many_partitions(env):
         check(torch, zr, idx_l, val_l, m, n_parts, seed=1)
 
 
+def test_wide_bins_few_partitions(env):
+    # A key range wide enough that bins grow past 1024 keys with at most 32
+    # partitions, plus dense runs of consecutive keys, so one bin's members
+    # span more than 32 bitmap words per partition.
+    torch, zr = env
+    rng = np.random.default_rng(13)
+    m = 1 << 29
+    idx_l = []
+    for r in range(4):
+        sparse = rng.integers(0, m, size=4000)
+        run = np.arange(1000 * r, 1000 * r + 6000)
+        run2 = np.arange(m - 5000, m - 5000 + 2500 * (r + 1) // 2)
+        idx_l.append(np.unique(np.concatenate([sparse, run, run2])).astype(np.int32))
+    val_l = [rng.standard_normal(a.size).astype(np.float32) for a in idx_l]
+    for n_parts in (32, 5, 1):
+        check(torch, zr, idx_l, val_l, m, n_parts, seed=n_parts)
+    check(torch, zr, idx_l, val_l, m, 7, seed=2, average=True)
+
+
+@pytest.mark.parametrize("n", [3, 4])
+def test_dense_bins(env, n):
+    # Many entries per 1024-key bin (about 40 % of the keys per rank), the
+    # regime where members are emitted partition by partition, with a
+    # ragged last bin.
+    torch, zr = env
+    m = 60_000 + 37
+    idx_l, val_l = workloads.random_coo(n, m, 25_000, seed=40 + n, shared=8_000)
+    for n_parts in (8, 32, 5, 1, 0):
+        check(torch, zr, idx_l, val_l, m, n_parts, seed=n_parts)
+    check(torch, zr, idx_l, val_l, m, 16, seed=3, average=True)
+
+
 def test_unsorted_input_sets_status(env):
     torch, zr = env
     good = np.array([1, 5, 9], np.int32)
