@@ -336,12 +336,36 @@ def timed_device(torch, W, steps, warmup):
     return total_ms, per
 
 
-def timed_e2e(torch, W, steps):
-    """Same step through the public API from pinned host buffers: every step
-    copies its inputs host->device and reads the results back."""
-    import numpy as np
+def second_slot(torch, W):
+    """A copy of the step's device buffers (dense ranks, sparse inputs,
+    workspaces and outputs), so that two steps can be in flight."""
+    import copy
 
     zr = W.zr
+    S = copy.copy(W)
+    if W.dense_on:
+        S.dense = torch.empty_like(W.dense)
+        S.bufs = [S.dense[r] for r in range(W.n)]
+    if W.sparse_on:
+        S.d_idx = [torch.empty_like(a) for a in W.d_idx]
+        S.d_val = [torch.empty_like(v) for v in W.d_val]
+        S.work = zr.SparseWorkspace(W.sn, W.m4, W.parts, sum(W.nnz), W.dev)
+        S.p_out_idx = torch.empty_like(W.p_out_idx)
+        S.p_out_val = torch.empty_like(W.p_out_val)
+        S.p_off = torch.empty_like(W.p_off)
+        S.p_ws = torch.empty_like(W.p_ws)
+    return S
+
+
+def timed_e2e(torch, W, steps):
+    """The step through the public API from pinned host buffers: every step
+    copies its inputs host->device and reads its results back.  Steps are
+    pipelined over two buffer slots and three streams (copy in, compute,
+    copy out), so step i's copy-in overlaps step i - 1's compute and copy-out;
+    a slot is refilled only after its last copy-out has finished."""
+    import numpy as np
+
+    slots = [W, second_slot(torch, W)]
     h_dense = torch.from_numpy(W.host_dense).pin_memory()
     h_idx = [torch.from_numpy(a).pin_memory() for a in W.host_idx]
     h_val = [torch.from_numpy(v).pin_memory() for v in W.host_val]
@@ -354,28 +378,46 @@ def timed_e2e(torch, W, steps):
     p_val = torch.empty(W.nnz[0], dtype=torch.float32).pin_memory()
     h2d = h_dense.numel() * 4 + sum(a.numel() * 8 for a in h_idx)
     d2h = W.m * 4 + W.union * 8 + (W.parts + 1) * 8 + W.nnz[0] * 8
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
-    def one(i):
-        W.dense.copy_(h_dense, non_blocking=True)
-        for r in range(W.n):
-            W.d_idx[r].copy_(h_idx[r], non_blocking=True)
-            W.d_val[r].copy_(h_val[r], non_blocking=True)
-        W.step(i)
-        out_dense.copy_(W.dense[0], non_blocking=True)
-        out_idx[:W.union].copy_(W.work.out_idx[:W.union], non_blocking=True)
-        out_val[:W.union].copy_(W.work.out_val[:W.union], non_blocking=True)
-        out_off.copy_(W.work.offsets[:W.parts + 1], non_blocking=True)
-        p_idx.copy_(W.p_out_idx, non_blocking=True)
-        p_val.copy_(W.p_out_val, non_blocking=True)
+    def run(first, count):
+        done = {}
+        for i in range(first, first + count):
+            S = slots[i % 2]
+            ev_in = torch.cuda.Event()
+            ev_comp = torch.cuda.Event()
+            ev_out = torch.cuda.Event()
+            with torch.cuda.stream(s_in):
+                if i - 2 in done:
+                    s_in.wait_event(done[i - 2])
+                S.dense.copy_(h_dense, non_blocking=True)
+                for r in range(W.sn):
+                    S.d_idx[r].copy_(h_idx[r], non_blocking=True)
+                    S.d_val[r].copy_(h_val[r], non_blocking=True)
+                ev_in.record(s_in)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(ev_in)
+                S.step(i)
+                ev_comp.record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp)
+                out_dense.copy_(S.dense[0], non_blocking=True)
+                out_idx[:W.union].copy_(S.work.out_idx[:W.union], non_blocking=True)
+                out_val[:W.union].copy_(S.work.out_val[:W.union], non_blocking=True)
+                out_off.copy_(S.work.offsets[:W.parts + 1], non_blocking=True)
+                p_idx.copy_(S.p_out_idx, non_blocking=True)
+                p_val.copy_(S.p_out_val, non_blocking=True)
+                ev_out.record(s_out)
+            done[i] = ev_out
+        return done
 
-    one(0)
+    run(0, 2)  # warm both slots
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for i in range(steps):
-        one(i + 1)
-    t1.record()
+    t0.record(s_in)
+    run(2, steps)
+    t1.record(s_out)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
     assert np.isfinite(float(out_dense[0]))
