@@ -120,10 +120,13 @@ __device__ __forceinline__ float apply_div(float x, const RingJob& J) {
   return x;
 }
 
-// AllReduce_Dropout: does the receiving rank with draw stream `stream` skip
-// element e?  (High 32 bits of SplitMix64 output e of that stream < T.)
-__device__ __forceinline__ bool drop_skip(uint64_t stream, int64_t e, uint64_t thr) {
-  return (splitmix_output(stream, (uint64_t)e) >> 32) < thr;
+// AllReduce_Dropout: the draw of element e on the receiving rank with draw
+// stream `stream` is one 32-bit half of SplitMix64 output e / 2 of that
+// stream, the high half for even e and the low half for odd e; the element
+// is skipped when the draw is below T.
+__device__ __forceinline__ uint32_t drop_draw(uint64_t stream, int64_t e) {
+  const uint64_t o = splitmix_output(stream, (uint64_t)e >> 1);
+  return (e & 1) ? (uint32_t)o : (uint32_t)(o >> 32);
 }
 
 struct RingShared {
@@ -172,7 +175,7 @@ __device__ __forceinline__ void ring_slice(const void* const* bufs, const RingJo
       float acc = E::load1(S.src[0], e);
       for (int t = 1; t < cnt; ++t) {
         const float x = E::load1(S.src[t], e);
-        if (!kDrop || !drop_skip(S.stream[t], e, J.drop_thr)) acc = __fadd_rn(acc, x);
+        if (!kDrop || (uint64_t)drop_draw(S.stream[t], e) >= J.drop_thr) acc = __fadd_rn(acc, x);
       }
       acc = apply_div(acc, J);
       for (int r = 0; r < nd; ++r) E::store1(S.dst[r], e, acc);
@@ -208,9 +211,20 @@ __device__ __forceinline__ void ring_slice(const void* const* bufs, const RingJo
           if (t + b < cnt) {
             float f[V];
             E::unpack(w[u][b], f);
+            // the vector's V elements start at an even index: their draws are
+            // the two halves of V / 2 consecutive outputs
+            uint32_t d[V];
+            if (kDrop) {
+#pragma unroll
+              for (int i = 0; i < V / 2; ++i) {
+                const uint64_t o = splitmix_output(S.stream[t + b], (uint64_t)(j * (V / 2) + i));
+                d[2 * i] = (uint32_t)(o >> 32);
+                d[2 * i + 1] = (uint32_t)o;
+              }
+            }
 #pragma unroll
             for (int q = 0; q < V; ++q) {
-              if (kDrop && drop_skip(S.stream[t + b], j * V + q, J.drop_thr)) continue;
+              if (kDrop && (uint64_t)d[q] < J.drop_thr) continue;
               acc[u][q] = __fadd_rn(acc[u][q], f[q]);
             }
           }

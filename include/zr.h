@@ -181,9 +181,10 @@ zr_status zr_skipreduce_buckets(const zr_bucket* buckets, int32_t n_buckets, int
  *            below T; T = ceil(p * 2^32) gives skip probability p (T = 0
  *            never skips, T = 2^32 always does).
  * seed, step generator seed shared by every rank, and the iteration count.
- * Draw of receiving rank r for element e (its index in the buffer): the high
- * 32 bits of output number e of SplitMix64 seeded with
- * s_r = (output number step * 64 + r of SplitMix64 seeded with seed).
+ * Draw of receiving rank r for element e (its index in the buffer): one
+ * 32-bit half of output number floor(e / 2) of SplitMix64 seeded with
+ * s_r = (output number step * 64 + r of SplitMix64 seeded with seed), the
+ * high half for even e and the low half for odd e.
  * Result: slice c (as in zr_ring_allreduce) is folded from its first sender,
  * rank c, whose value is always kept; rank c + t (t = 1 .. n-1, mod n) adds
  * its value unless its draw for e is below T.  Then divided by n when

@@ -43,10 +43,10 @@ skipped element forwards the received value unchanged, otherwise it forwards
 local + received.  The rank that first sends a slice is never asked, so its
 value is always in the sum.  The pages draw from cuRAND; here the draw of
 receiving rank r for element e (its index in the tensor) in iteration
-``step`` is the top 32 bits of output number e of SplitMix64 seeded with
-``dropout_stream(seed, step, r)`` (output number step*64 + r of
-SplitMix64(seed)), and the element is skipped when those bits are below the
-integer threshold T (T = ceil(p * 2**32) for skip probability p, so T = 0
+``step`` is one 32-bit half of output number e // 2 of SplitMix64 seeded
+with ``dropout_stream(seed, step, r)`` (output number step*64 + r of
+SplitMix64(seed)): the high half for even e, the low half for odd e.  The
+element is skipped when the draw is below the integer threshold T (T = ceil(p * 2**32) for skip probability p, so T = 0
 never skips and T = 2**32 always does).
 
 RS-only (15-642 notes, "ZeRO Stage 2": the AllReduce is replaced by a
@@ -102,12 +102,15 @@ def dropout_stream(seed, step, r):
 def dropout_skips(seed, step, r, elems, threshold):
     """Boolean array: does rank r skip each element index in ``elems``?
 
-    The element's draw is the top 32 bits of output number e of
-    SplitMix64(dropout_stream(seed, step, r)); it is skipped when the draw is
-    below ``threshold`` (an integer in [0, 2**32]).
+    The element's draw is one 32-bit half of output number e // 2 of
+    SplitMix64(dropout_stream(seed, step, r)): the high half for even e, the
+    low half for odd e.  The element is skipped when the draw is below
+    ``threshold`` (an integer in [0, 2**32]).
     """
     s = dropout_stream(seed, step, r)
-    draws = splitmix.outputs(s, np.asarray(elems, dtype=np.int64)) >> np.uint64(32)
+    e = np.asarray(elems, dtype=np.int64)
+    out = splitmix.outputs(s, e >> 1)
+    draws = np.where((e & 1) == 1, out & np.uint64(0xFFFFFFFF), out >> np.uint64(32))
     return draws.astype(np.int64) < threshold
 
 

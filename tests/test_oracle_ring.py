@@ -322,6 +322,34 @@ def test_dropout_skip_rate_matches_probability():
     assert not np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("p", [0.5, 0.3])
+def test_dropout_neighbour_draws_independent(p):
+    # Two neighbouring elements share one 64-bit generator output (its two
+    # halves); their skips must still be independent: the joint skip rate of
+    # each pair (2i, 2i+1), and of the pairs straddling two outputs
+    # (2i+1, 2i+2), is p^2 within 5 sigma.  Drawing both elements from the
+    # same half would give p; the two halves swapped or taken from
+    # different outputs would fail the element-by-element pins above.
+    m = 1 << 16
+    thr = ring.dropout_threshold(p)
+    s = ring.dropout_skips(11, 2, 3, np.arange(m), thr)
+    q = p * p
+    sigma = (q * (1 - q) / (m // 2)) ** 0.5
+    same = (s[0::2] & s[1::2]).mean()
+    straddle = (s[1:-1:2] & s[2::2]).mean()
+    assert abs(same - q) < 5 * sigma, same
+    assert abs(straddle - q) < 5 * sigma, straddle
+    # the even element's draw is the high half of output e / 2, the odd
+    # element's the low half (the generator itself is pinned by its
+    # published known-answer vectors)
+    from oracle import splitmix
+    st = ring.dropout_stream(11, 2, 3)
+    for e in (0, 1, 6, 7, 1001):
+        o = splitmix.output(st, e // 2)
+        draw = (o & 0xFFFFFFFF) if e % 2 else (o >> 32)
+        assert bool(ring.dropout_skips(11, 2, 3, [e], thr)[0]) == (draw < thr)
+
+
 # ----------------------------------------------------------------- RS-only
 @pytest.mark.parametrize("n,k,o", [(2, 0, 0), (4, 1, 2), (5, 3, 1), (8, 4, 7)])
 def test_rs_only_holder_slices_equal_full_ring(n, k, o):
