@@ -15,10 +15,11 @@
 //           element 32j + l of the word's index set and a ballot forms word j;
 //           the 32 words leave as one coalesced store.
 //   decode: per tile of 1024 words, a popcount pass and a one-CTA scan give
-//           every tile its first output position; then each warp walks its
-//           words, and lane l of word j writes I_p[32j + l] (when bit l is
-//           set) at the word's base plus the popcount of the lower bits, so a
-//           word's keys leave as one contiguous store.
+//           every tile its first output position; then each warp takes 32
+//           words at a time, lane l word j = g0 + l, and the lane writes
+//           I_p[32j + b] for every set bit b of its word at the word's output
+//           base (a prefix of the popcounts over the lanes) plus the rank of
+//           b among the word's set bits, up to 4 gathers in flight.
 // Every index taken from the inputs is range-checked before it addresses
 // memory; every output position is checked against the output capacity.
 
@@ -39,12 +40,6 @@ constexpr int kScanThreads = 1024;
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 __device__ __forceinline__ void flag(int32_t* status, int code) { atomicCAS(status, 0, code); }
-
-__device__ __forceinline__ unsigned lanemask_lt() {
-  unsigned m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
 
 int64_t words_bound(int64_t m, int parts) { return (m + 31) / 32 + parts; }
 
@@ -253,7 +248,6 @@ hb_decode_kernel(const int32_t* sets, const int64_t* set_off, int parts, const u
   __shared__ int32_t s_wsum[kWarps];
   load_offsets(woff_ws, set_off, parts, s_woff, s_soff);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned lt = lanemask_lt();
   const int64_t total = s_woff[parts];
   const int64_t tiles = (total + kTileWords - 1) / kTileWords;
   constexpr int kPerWarp = kTileWords / kWarps;
@@ -267,36 +261,45 @@ hb_decode_kernel(const int32_t* sets, const int64_t* set_off, int parts, const u
     __syncthreads();
     long long run = tbase[t];
     for (int w = 0; w < warp; ++w) run += s_wsum[w];
+    // Lane l takes word g0 + l and walks its set bits: up to 4 gathers of
+    // index-set elements in flight (read-only loads), then their stores at
+    // the word's output base plus the bits' rank.
     int p = 0;
     for (int64_t g0 = wlo; g0 < whi; g0 += 32) {
-      const uint32_t mine = g0 + lane < whi ? bits[g0 + lane] : 0u;
+      const int64_t g = g0 + lane;
+      const uint32_t mine = g < whi ? bits[g] : 0u;
       const int cnt = __popc(mine);
       const int incl = warp_incl_scan(cnt);
-      {
-        constexpr int u0 = 0;
-        int32_t key[32];
-        int rel[32];  // output position relative to run; -1: nothing to write
+      if (mine) {
+        p = word_part(s_woff, parts, g, p);
+        const int64_t set_lo = s_soff[p];
+        const int64_t set_n = s_soff[p + 1] - set_lo;
+        const int64_t pos0 = (g - s_woff[p]) * 32;
+        long long o = run + incl - cnt;
+        uint32_t w = mine;
+        while (w) {
+          int32_t key[4];
+          long long at[4];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const int64_t g = g0 + u0 + u;
-          const uint32_t word = __shfl_sync(0xffffffffu, mine, u0 + u);
-          const int before = __shfl_sync(0xffffffffu, incl - cnt, u0 + u);
-          rel[u] = -1;
-          if (g < whi && ((word >> lane) & 1u)) {
-            p = word_part(s_woff, parts, g, p);
-            const int64_t pos = (g - s_woff[p]) * 32 + lane;
-            const int r = before + __popc(word & lt);
-            if (pos < s_soff[p + 1] - s_soff[p] && run + r < out_cap) {
-              key[u] = sets[s_soff[p] + pos];
-              rel[u] = r;
-            } else {
-              flag(status, ZR_ERR_INVALID_ARG);  // a bit past the set's end, or no room
+          for (int i = 0; i < 4; ++i) {
+            at[i] = -1;
+            if (w) {
+              const int bit = __ffs(w) - 1;
+              w &= w - 1;
+              const int64_t pos = pos0 + bit;
+              if (pos < set_n && o < out_cap) {
+                key[i] = __ldg(sets + set_lo + pos);
+                at[i] = o;
+              } else {
+                flag(status, ZR_ERR_INVALID_ARG);  // a bit past the set's end, or no room
+              }
+              ++o;
             }
           }
-        }
 #pragma unroll
-        for (int u = 0; u < 32; ++u)
-          if (rel[u] >= 0) out[run + rel[u]] = key[u];
+          for (int i = 0; i < 4; ++i)
+            if (at[i] >= 0) out[at[i]] = key[i];
+        }
       }
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
