@@ -57,7 +57,7 @@ TRAFFIC = {
 # Kernels of this library launched per component per step (the status-word
 # memset of the sparse path is a runtime memset, not counted).
 LAUNCHES = {"ring": 1, "skip": 1, "sparse": 5, "partition": 3, "dropout": 1, "buckets": 1,
-            "hb_encode": 3, "hb_decode": 4, "hb_sets": 4}
+            "hb_encode": 3, "hb_decode": 3, "hb_sets": 4}
 
 
 def torch_stream(torch):

@@ -60,21 +60,28 @@ HbLayout hb_layout(int64_t m, int parts) {
   return L;
 }
 
-// woff[p] = sum_{q < p} ceil(|I_q| / 32), from the index-set offsets.  One
-// thread; parts <= 256.  Offsets that do not describe index sets of [0, m)
-// (not starting at 0, not ending at m, or decreasing) are flagged and give
-// empty bitmaps, so the later kernels touch nothing.
-__global__ void hb_word_offsets_kernel(const int64_t* set_off, int parts, int64_t m,
-                                       int64_t* woff_ws, int64_t* woff_out, int32_t* status) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+// woff[p] = sum_{q < p} ceil(|I_q| / 32), from the index-set offsets (one
+// thread; parts <= 256).  Offsets that do not describe index sets of [0, m)
+// (not starting at 0, not ending at m, or decreasing) give empty bitmaps, so
+// the later kernels touch nothing; the function returns false for them.
+__device__ bool word_offsets(const int64_t* set_off, int parts, int64_t m, int64_t* woff) {
   bool ok = set_off[0] == 0 && set_off[parts] == m;
   for (int p = 0; p < parts; ++p) ok = ok && set_off[p + 1] >= set_off[p];
   int64_t acc = 0;
   for (int p = 0; p <= parts; ++p) {
-    woff_ws[p] = acc;
-    if (woff_out) woff_out[p] = acc;
+    woff[p] = acc;
     if (ok && p < parts) acc += (set_off[p + 1] - set_off[p] + 31) / 32;
   }
+  return ok;
+}
+
+// The encoder's word offsets, also returned to the caller (woff_out).
+__global__ void hb_word_offsets_kernel(const int64_t* set_off, int parts, int64_t m,
+                                       int64_t* woff_ws, int64_t* woff_out, int32_t* status) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  const bool ok = word_offsets(set_off, parts, m, woff_ws);
+  if (woff_out)
+    for (int p = 0; p <= parts; ++p) woff_out[p] = woff_ws[p];
   if (!ok) flag(status, ZR_ERR_INVALID_ARG);
 }
 
@@ -166,9 +173,21 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
 }
 
 __global__ void __launch_bounds__(kThreads)
-hb_tile_count_kernel(const uint32_t* bits, const int64_t* woff_ws, int parts, int32_t* tcnt) {
+hb_tile_count_kernel(const uint32_t* bits, const int64_t* set_off, int parts, int64_t m,
+                     int64_t* woff_ws, int32_t* tcnt, int32_t* status) {
   __shared__ int32_t s_sum[kWarps];
-  const int64_t total = woff_ws[parts];
+  __shared__ int64_t s_woff[ZR_MAX_PARTS + 1];
+  // every CTA derives the word offsets; CTA 0 also stores them for the scan
+  // and the decode
+  if (threadIdx.x == 0) {
+    const bool ok = word_offsets(set_off, parts, m, s_woff);
+    if (blockIdx.x == 0) {
+      for (int p = 0; p <= parts; ++p) woff_ws[p] = s_woff[p];
+      if (!ok) flag(status, ZR_ERR_INVALID_ARG);
+    }
+  }
+  __syncthreads();
+  const int64_t total = s_woff[parts];
   const int64_t tiles = (total + kTileWords - 1) / kTileWords;
   for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
     const int64_t lo = t * kTileWords, hi = min(lo + kTileWords, total);
@@ -220,23 +239,16 @@ hb_scan_kernel(const uint32_t* bits, const int64_t* woff_ws, int parts, const in
   if (carry > out_cap && tid == 0) flag(status, ZR_ERR_CAPACITY);
   __syncthreads();
   // key offset of partition p: the set bits before its first word = its
-  // tile's base plus the popcount of the tile's words before it (the whole
-  // CTA sums those, one partition at a time)
-  for (int p = 0; p <= parts; ++p) {
+  // tile's base plus the popcount of the tile's words before it; one warp
+  // per partition (the tile bases above are visible after the barrier)
+  for (int p = warp; p <= parts; p += kScanThreads / 32) {
     const int64_t w = woff_ws[p];
     const int64_t t = w / kTileWords;
     int c = 0;
     if (t < tiles)
-      for (int64_t g = t * kTileWords + tid; g < w; g += kScanThreads) c += __popc(bits[g]);
+      for (int64_t g = t * kTileWords + lane; g < w; g += 32) c += __popc(bits[g]);
     for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-    if (lane == 0) s_warp[warp] = c;
-    __syncthreads();
-    if (tid == 0) {
-      long long k = t < tiles ? tbase[t] : carry;
-      for (int i = 0; i < kScanThreads / 32; ++i) k += s_warp[i];
-      key_off[p] = k;
-    }
-    __syncthreads();
+    if (lane == 0) key_off[p] = (t < tiles ? tbase[t] : carry) + c;
   }
 }
 
@@ -350,10 +362,10 @@ zr_status hash_bitmap_decode_launch(const int32_t* sets, const int64_t* d_set_of
   int64_t* tbase = reinterpret_cast<int64_t*>(w + L.tbase);
   if (cudaMemsetAsync(w, 0, 256, stream) != cudaSuccess) return ZR_ERR_CUDA;
   // Partition p's words start where the encoder put them: the offsets follow
-  // from the index sets alone.
-  hb_word_offsets_kernel<<<1, 32, 0, stream>>>(d_set_offsets, n_parts, m, woff, nullptr, status);
+  // from the index sets alone (the tile count kernel derives them).
   const int64_t tiles = (words_bound(m, n_parts) + kTileWords - 1) / kTileWords;
-  hb_tile_count_kernel<<<grid_for(tiles, 4), kThreads, 0, stream>>>(bits, woff, n_parts, tcnt);
+  hb_tile_count_kernel<<<grid_for(tiles, 4), kThreads, 0, stream>>>(bits, d_set_offsets, n_parts,
+                                                                   m, woff, tcnt, status);
   hb_scan_kernel<<<1, kScanThreads, 0, stream>>>(bits, woff, n_parts, tcnt, tbase, d_key_offsets,
                                                  out_cap, status);
   hb_decode_kernel<<<grid_for(tiles, 4), kThreads, 0, stream>>>(
