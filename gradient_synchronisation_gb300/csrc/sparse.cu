@@ -957,32 +957,96 @@ PartLayout part_layout(int64_t tiles, int parts) {
 
 // kIdentity: the input is the index range itself (position i holds index i,
 // no values) -- the partition that builds Zen's index sets I_p.
-template <bool kIdentity>
+//
+// Up to 32 partitions (kBallot) a warp splits 32 entries at a time with
+// ceil(log2 P) ballots of the partition bits: lane l learns which lanes share
+// its partition (its rank among them) and lane q how many entries of the 32
+// fall in partition q, so counts stay in registers; above 32 partitions a
+// match_any groups the lanes of one partition.
+
+// Lanes whose partition equals the lane index q (kBits partition bits): the
+// AND over the bits of the matching ballots, restricted to live lanes.
+template <int kBits>
+__device__ __forceinline__ unsigned part_lanes(unsigned live_mask, int p, int q) {
+  unsigned m = live_mask;
+#pragma unroll
+  for (int i = 0; i < kBits; ++i) {
+    const unsigned bi = __ballot_sync(0xffffffffu, (p >> i) & 1);
+    m &= ((q >> i) & 1) ? bi : ~bi;
+  }
+  return m;
+}
+
+// Both masks of one step: lanes in the caller's own partition p (same) and
+// lanes in partition q = the lane index (mine_q), from one set of ballots.
+template <int kBits>
+__device__ __forceinline__ void part_masks(unsigned live_mask, int p, unsigned& same,
+                                           unsigned& mine_q) {
+  const int q = threadIdx.x & 31;
+  same = live_mask;
+  mine_q = live_mask;
+#pragma unroll
+  for (int i = 0; i < kBits; ++i) {
+    const unsigned bi = __ballot_sync(0xffffffffu, (p >> i) & 1);
+    same &= ((p >> i) & 1) ? bi : ~bi;
+    mine_q &= ((q >> i) & 1) ? bi : ~bi;
+  }
+}
+
+// kBits: the partitions' bit count when at most 32 (ballots), -1 above
+// (match_any).
+template <bool kIdentity, int kBits>
 __global__ void __launch_bounds__(kPartThreads)
 part_count_kernel(const int32_t* idx, int64_t nnz, int64_t tiles, H0 h, int parts,
                   int32_t* cnt_g) {
+  constexpr int kPW = kPartThreads / 32;
+  constexpr int kPerWarp = kPartTile / kPW;
   __shared__ int32_t cnt[ZR_MAX_PARTS];
-  const int tid = threadIdx.x;
+  __shared__ int32_t wcnt[kPW][32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const H0 hash = h;
+  constexpr bool kBallot = kBits >= 0;
   for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-    for (int q = tid; q < parts; q += kPartThreads) cnt[q] = 0;
-    __syncthreads();
-    const int64_t lo = t * kPartTile, hi = min(lo + kPartTile, nnz);
-    for (int64_t i = lo + tid; i < lo + kPartTile; i += kPartThreads) {
-      const bool live = i < hi;
-      const int p = live ? (int)hash(kIdentity ? (uint32_t)i : (uint32_t)idx[i]) : parts;
-      const unsigned peers = __match_any_sync(0xffffffffu, p);
-      if (live && (peers & lanemask_lt()) == 0) atomicAdd(&cnt[p], __popc(peers));
+    const int64_t hi = min(t * kPartTile + kPartTile, nnz);
+    if (kBallot) {
+      const int64_t lo = t * kPartTile + (int64_t)warp * kPerWarp;
+      int c = 0;  // lane q: entries of partition q among the warp's
+#pragma unroll
+      for (int j = 0; j < kPerWarp; j += 32) {
+        const int64_t i = lo + j + lane;
+        const bool live = i < hi;
+        const int p = live ? (int)hash(kIdentity ? (uint32_t)i : (uint32_t)idx[i]) : 0;
+        c += __popc(part_lanes<kBallot ? kBits : 0>(__ballot_sync(0xffffffffu, live), p, lane));
+      }
+      wcnt[warp][lane] = c;
+      __syncthreads();
+      for (int q = tid; q < parts; q += kPartThreads) {
+        int s = 0;
+#pragma unroll
+        for (int w = 0; w < kPW; ++w) s += wcnt[w][q];
+        __stcg(cnt_g + (size_t)q * tiles + t, s);
+      }
+      __syncthreads();
+    } else {
+      for (int q = tid; q < parts; q += kPartThreads) cnt[q] = 0;
+      __syncthreads();
+      for (int64_t i = t * kPartTile + tid; i < t * kPartTile + kPartTile; i += kPartThreads) {
+        const bool live = i < hi;
+        const int p = live ? (int)hash(kIdentity ? (uint32_t)i : (uint32_t)idx[i]) : parts;
+        const unsigned peers = __match_any_sync(0xffffffffu, p);
+        if (live && (peers & lanemask_lt()) == 0) atomicAdd(&cnt[p], __popc(peers));
+      }
+      __syncthreads();
+      for (int q = tid; q < parts; q += kPartThreads)
+        __stcg(cnt_g + (size_t)q * tiles + t, cnt[q]);
+      __syncthreads();
     }
-    __syncthreads();
-    for (int q = tid; q < parts; q += kPartThreads) __stcg(cnt_g + (size_t)q * tiles + t, cnt[q]);
-    __syncthreads();
   }
 }
 
 // Each warp owns kPartTile / warps consecutive entries of the tile and walks
 // them 32 at a time, so the entries of one partition leave in input order.
-template <bool kIdentity>
+template <bool kIdentity, int kBits>
 __global__ void __launch_bounds__(kPartThreads)
 part_write_kernel(const int32_t* idx, const float* val, int64_t nnz, int64_t tiles, H0 h,
                   int parts, const long long* excl_g, const long long* tot_g, int32_t* out_idx,
@@ -992,46 +1056,89 @@ part_write_kernel(const int32_t* idx, const float* val, int64_t nnz, int64_t til
   __shared__ long long offs[ZR_MAX_PARTS + 1];
   constexpr int kPW = kPartThreads / 32;
   constexpr int kPerWarp = kPartTile / kPW;
+  constexpr int kSteps = kPerWarp / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt = lanemask_lt();
   const H0 hash = h;
+  constexpr bool kBallot = kBits >= 0;
   load_partition_offsets(tot_g, parts, offs, d_offsets, nullptr);
   for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-    for (int q = threadIdx.x; q < kPW * parts; q += kPartThreads) wbase[q] = 0;
-    __syncthreads();
     const int64_t lo = t * kPartTile + (int64_t)warp * kPerWarp;
     const int64_t hi = min(t * kPartTile + kPartTile, nnz);
-    for (int j = 0; j < kPerWarp; j += 32) {
-      const int64_t i = lo + j + lane;
-      const bool live = i < hi;
-      const int p = live ? (int)hash(kIdentity ? (uint32_t)i : (uint32_t)idx[i]) : parts;
-      const unsigned peers = __match_any_sync(0xffffffffu, p);
-      if (live && (peers & lanemask_lt()) == 0) wbase[warp * parts + p] += __popc(peers);
-      __syncwarp();
-    }
-    __syncthreads();
-    for (int q = threadIdx.x; q < parts; q += kPartThreads) {
-      long long run = offs[q] + __ldcg(excl_g + (size_t)q * tiles + t);
-      for (int w = 0; w < kPW; ++w) {
-        const long long c = wbase[w * parts + q];
-        wbase[w * parts + q] = run;
-        run += c;
+    if (kBallot) {
+      // the warp's keys and partitions stay in registers between the passes
+      int32_t key[kSteps];
+      int part[kSteps];
+      int c = 0;
+#pragma unroll
+      for (int s = 0; s < kSteps; ++s) {
+        const int64_t i = lo + s * 32 + lane;
+        const bool live = i < hi;
+        key[s] = live ? (kIdentity ? (int32_t)i : idx[i]) : 0;
+        part[s] = live ? (int)hash((uint32_t)key[s]) : 0;
+        c += __popc(
+            part_lanes<kBallot ? kBits : 0>(__ballot_sync(0xffffffffu, live), part[s], lane));
       }
-    }
-    __syncthreads();
-    for (int j = 0; j < kPerWarp; j += 32) {
-      const int64_t i = lo + j + lane;
-      const bool live = i < hi;
-      const int32_t key = live ? (kIdentity ? (int32_t)i : idx[i]) : 0;
-      const int p = live ? (int)hash((uint32_t)key) : parts;
-      const unsigned peers = __match_any_sync(0xffffffffu, p);
-      if (live) {
-        const long long dst = wbase[warp * parts + p] + __popc(peers & lanemask_lt());
-        out_idx[dst] = key;
-        if (!kIdentity) out_val[dst] = val[i];
+      long long* wc = wbase;  // [warp][32] counts, then bases
+      wc[warp * 32 + lane] = c;
+      __syncthreads();
+      // lane q: partition q's first output position for this warp's entries
+      long long run = 0;
+      if (lane < parts) {
+        run = offs[lane] + __ldcg(excl_g + (size_t)lane * tiles + t);
+        for (int w = 0; w < warp; ++w) run += wc[w * 32 + lane];
       }
-      __syncwarp();
-      if (live && (peers & lanemask_lt()) == 0) wbase[warp * parts + p] += __popc(peers);
-      __syncwarp();
+      __syncthreads();
+#pragma unroll
+      for (int s = 0; s < kSteps; ++s) {
+        const int64_t i = lo + s * 32 + lane;
+        const bool live = i < hi;
+        unsigned same, mine_q;
+        part_masks<kBallot ? kBits : 0>(__ballot_sync(0xffffffffu, live), part[s], same, mine_q);
+        const long long at = __shfl_sync(0xffffffffu, run, part[s]);
+        if (live) {
+          const long long dst = at + __popc(same & lt);
+          out_idx[dst] = key[s];
+          if (!kIdentity) out_val[dst] = val[i];
+        }
+        run += __popc(mine_q);
+      }
+    } else {
+      for (int q = threadIdx.x; q < kPW * parts; q += kPartThreads) wbase[q] = 0;
+      __syncthreads();
+      for (int j = 0; j < kPerWarp; j += 32) {
+        const int64_t i = lo + j + lane;
+        const bool live = i < hi;
+        const int p = live ? (int)hash(kIdentity ? (uint32_t)i : (uint32_t)idx[i]) : parts;
+        const unsigned peers = __match_any_sync(0xffffffffu, p);
+        if (live && (peers & lt) == 0) wbase[warp * parts + p] += __popc(peers);
+        __syncwarp();
+      }
+      __syncthreads();
+      for (int q = threadIdx.x; q < parts; q += kPartThreads) {
+        long long run = offs[q] + __ldcg(excl_g + (size_t)q * tiles + t);
+        for (int w = 0; w < kPW; ++w) {
+          const long long c = wbase[w * parts + q];
+          wbase[w * parts + q] = run;
+          run += c;
+        }
+      }
+      __syncthreads();
+      for (int j = 0; j < kPerWarp; j += 32) {
+        const int64_t i = lo + j + lane;
+        const bool live = i < hi;
+        const int32_t key = live ? (kIdentity ? (int32_t)i : idx[i]) : 0;
+        const int p = live ? (int)hash((uint32_t)key) : parts;
+        const unsigned peers = __match_any_sync(0xffffffffu, p);
+        if (live) {
+          const long long dst = wbase[warp * parts + p] + __popc(peers & lt);
+          out_idx[dst] = key;
+          if (!kIdentity) out_val[dst] = val[i];
+        }
+        __syncwarp();
+        if (live && (peers & lt) == 0) wbase[warp * parts + p] += __popc(peers);
+        __syncwarp();
+      }
     }
     __syncthreads();
   }
@@ -1176,7 +1283,7 @@ DeviceInfo* device_info() {
           return nullptr;
     }
     d.count_per_sm = per_sm((const void*)bin_count_kernel, kBinThreads, 0);
-    d.part_count_per_sm = per_sm((const void*)part_count_kernel<false>, kPartThreads, 0);
+    d.part_count_per_sm = per_sm((const void*)part_count_kernel<false, 3>, kPartThreads, 0);
     d.ready = 1;
   }
   return &d;
@@ -1333,6 +1440,27 @@ size_t partition_workspace_bytes(int64_t nnz, int n_parts) {
 }
 
 namespace {
+// The count (count = true) or write kernel for nbits partition bits (-1:
+// more than 32 partitions).
+template <bool kIdentity, int kB>
+const void* part_kernel_bits(bool count) {
+  return count ? (const void*)part_count_kernel<kIdentity, kB>
+               : (const void*)part_write_kernel<kIdentity, kB>;
+}
+
+template <bool kIdentity>
+const void* part_kernel(bool count, int nbits) {
+  switch (nbits) {
+    case 0: return part_kernel_bits<kIdentity, 0>(count);
+    case 1: return part_kernel_bits<kIdentity, 1>(count);
+    case 2: return part_kernel_bits<kIdentity, 2>(count);
+    case 3: return part_kernel_bits<kIdentity, 3>(count);
+    case 4: return part_kernel_bits<kIdentity, 4>(count);
+    case 5: return part_kernel_bits<kIdentity, 5>(count);
+    default: return part_kernel_bits<kIdentity, -1>(count);
+  }
+}
+
 template <bool kIdentity>
 zr_status partition_run(const int32_t* idx, const float* val, int64_t nnz, int n_parts,
                         uint64_t part_seed, int32_t* out_idx, float* out_val,
@@ -1353,8 +1481,16 @@ zr_status partition_run(const int32_t* idx, const float* val, int64_t nnz, int n
   if (tiles > 0x7fffffff) return ZR_ERR_UNSUPPORTED;
   DeviceInfo* dinfo = device_info();
   if (!dinfo) return ZR_ERR_CUDA;
-  part_count_kernel<kIdentity><<<(unsigned)grid_for(tiles, dinfo->part_count_per_sm),
-                                 kPartThreads, 0, stream>>>(idx, nnz, tiles, h, n_parts, cnt);
+  // ballots on ceil(log2 P) partition bits up to 32 partitions, match_any above
+  const int nbits = n_parts > 32 ? -1 : (n_parts > 1 ? 32 - __builtin_clz((unsigned)n_parts - 1) : 0);
+  const bool ballot = nbits >= 0;
+  const unsigned count_grid = (unsigned)grid_for(tiles, dinfo->part_count_per_sm);
+  const void* count_fn = part_kernel<kIdentity>(true, nbits);
+  void* count_args[] = {(void*)&idx, (void*)&nnz, (void*)&tiles, (void*)&h, (void*)&n_parts,
+                        (void*)&cnt};
+  if (cudaLaunchKernel(count_fn, dim3(count_grid), dim3(kPartThreads), count_args, 0, stream) !=
+      cudaSuccess)
+    return ZR_ERR_CUDA;
   const int chunks = (int)((tiles + kChunkBins - 1) >> kChunkLog);
   // With one chunk the scan needs no carry, so the chunk sums are skipped.
   if (chunks > 1)
@@ -1362,9 +1498,18 @@ zr_status partition_run(const int32_t* idx, const float* val, int64_t nnz, int n
         cnt, (int)tiles, ctot);
   bin_scan_kernel<<<dim3((unsigned)chunks, (unsigned)n_parts), kScanThreads, 0, stream>>>(
       cnt, ctot, (int)tiles, excl, tot);
-  const size_t smem = (size_t)(kPartThreads / 32) * n_parts * sizeof(long long);
-  part_write_kernel<kIdentity><<<(unsigned)grid_for(tiles, 8), kPartThreads, smem, stream>>>(
-      idx, val, nnz, tiles, h, n_parts, excl, tot, out_idx, out_val, d_offsets);
+  // per-warp counts and bases: 32 lanes (ballot) or one per partition
+  const size_t smem = (size_t)(kPartThreads / 32) * (ballot ? 32 : n_parts) * sizeof(long long);
+  const unsigned write_grid = (unsigned)grid_for(tiles, 8);
+  const void* write_fn = part_kernel<kIdentity>(false, nbits);
+  const long long* excl_c = excl;
+  const long long* tot_c = tot;
+  void* write_args[] = {(void*)&idx, (void*)&val, (void*)&nnz, (void*)&tiles, (void*)&h,
+                        (void*)&n_parts, (void*)&excl_c, (void*)&tot_c, (void*)&out_idx,
+                        (void*)&out_val, (void*)&d_offsets};
+  if (cudaLaunchKernel(write_fn, dim3(write_grid), dim3(kPartThreads), write_args, smem, stream) !=
+      cudaSuccess)
+    return ZR_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
 }
 }  // namespace

@@ -164,7 +164,7 @@ def test_partition_entry(env):
     for nnz in (0, 1, 31, 4096, 4097, 100_003):
         idx = rng.integers(0, 1 << 30, size=nnz).astype(np.int32)  # any order, repeats allowed
         val = rng.standard_normal(nnz).astype(np.float32)
-        for n_parts in (1, 3, 16, 256):
+        for n_parts in (1, 2, 3, 5, 16, 32, 33, 256):
             d_i = torch.from_numpy(idx).cuda()
             d_v = torch.from_numpy(val).cuda()
             oi, ov, off = zr.partition(d_i, d_v, n_parts, part_seed=n_parts)
