@@ -57,7 +57,7 @@ TRAFFIC = {
 # Kernels of this library launched per component per step (the status-word
 # memset of the sparse path is a runtime memset, not counted).
 LAUNCHES = {"ring": 1, "skip": 1, "sparse": 5, "partition": 3, "dropout": 1, "buckets": 1,
-            "hb_encode": 3, "hb_decode": 3, "hb_sets": 4}
+            "hb_encode": 3, "hb_decode": 3, "hb_sets": 4, "densify": 2}
 
 
 def torch_stream(torch):
@@ -73,6 +73,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only", choices=("ring", "skip", "sparse", "partition", "dropout", "buckets",
+                                       "densify",
                                        "hb_encode", "hb_decode", "hb_sets"),
                     default=None,
                     help="profiling: time one component alone (prints a profiling line, not the "
@@ -207,7 +208,8 @@ class Workload:
         self.seed = c2["skip_seed"]
         self.dense_on = any(c in self.components for c in ("ring", "skip", "dropout", "buckets"))
         self.sparse_on = any(c in self.components
-                             for c in ("sparse", "partition", "hb_encode", "hb_decode", "hb_sets"))
+                             for c in ("sparse", "partition", "hb_encode", "hb_decode", "hb_sets",
+                                       "densify"))
         if self.dense_on:
             if dense_m:
                 self.host_dense = workloads.dense_f32_per_rank(self.n, self.m, c2["sigma"], 200)
@@ -247,6 +249,13 @@ class Workload:
                                 work=self.work)
             torch.cuda.synchronize()
             self.union = int(self.work.out_nnz.item())
+            if "densify" in self.components:
+                # Zen's densification measurement: union sizes of every group
+                # of 2^L consecutive ranks, for the scheme choice
+                self.dn_ws = torch.empty(zr.zr_densification_workspace_size(self.sn, self.m4),
+                                         dtype=torch.uint8, device=dev)
+                self.dn_out = torch.empty(self.sn.bit_length(), dtype=torch.int64, device=dev)
+                self.dn_ptrs = [a.data_ptr() for a in self.d_idx]
             if any(c in self.components for c in ("hb_encode", "hb_decode", "hb_sets")):
                 # Zen's Pull: every server's hash bitmap of the union's keys
                 self.hb = zr.HashBitmap(self.m4, self.parts, self.part_seed)
@@ -278,6 +287,8 @@ class Workload:
             out["hb_decode"] = words * 4 + self.union * 4 * 2 + (self.parts + 1) * 8
             # index sets: every index written once
             out["hb_sets"] = self.m4 * 4 + (self.parts + 1) * 8
+            # densification: every key read once, the log2(n) + 1 counts out
+            out["densify"] = sum(self.nnz) * 4 + self.sn.bit_length() * 8
         return {c: out[c] for c in self.components}
 
     def run(self, name, i):
@@ -299,6 +310,10 @@ class Workload:
             zr.zr_hash_index_sets(self.m4, self.parts, self.part_seed, self.hb.sets.data_ptr(),
                                   self.hb.offsets.data_ptr(), self.hb_sets_ws.data_ptr(),
                                   self.hb_sets_ws.numel(), torch_stream(self.torch))
+        elif name == "densify":
+            zr.zr_densification(self.dn_ptrs, self.nnz, self.sn, self.m4, self.dn_out.data_ptr(),
+                                self.dn_ws.data_ptr(), self.dn_ws.numel(),
+                                torch_stream(self.torch))
         elif name == "sparse":
             zr.sparse_aggregate(self.d_idx, self.d_val, self.m4, self.parts, self.part_seed,
                                 work=self.work)

@@ -1151,8 +1151,11 @@ part_write_kernel(const int32_t* idx, const float* val, int64_t nnz, int64_t til
 // with a holder, level L folds the mask so that bit i * 2^L holds the OR of
 // group i's 2^L ranks, and the set bits at multiples of 2^L count the
 // groups of size 2^L whose union holds the key.  Sums per level stay in
-// registers until one atomic per warp at the end.
+// registers until one atomic per warp at the end (per-CTA partial sums and a
+// one-CTA reduction measured slower on C4: the extra launch costs more than
+// the atomics).
 constexpr int kDensWarps = 4;
+constexpr int kDensChunks = 8;
 
 __device__ __forceinline__ unsigned long long group_sel(int level) {
   switch (level) {
@@ -1174,9 +1177,9 @@ densify_kernel(const __grid_constant__ Lists lists, int n, int logn, int log_w, 
   unsigned long long* mk = masks_all + (size_t)warp * W;
   unsigned long long cnt[6] = {0, 0, 0, 0, 0, 0};
   const int nwarps = gridDim.x * kDensWarps;
+  for (int i = lane; i < W; i += 32) mk[i] = 0ull;  // then cleared as it is read
   for (int b = blockIdx.x * kDensWarps + warp; b < bins; b += nwarps) {
     const uint32_t base = (uint32_t)b << log_w;
-    for (int i = lane; i < W; i += 32) mk[i] = 0ull;
     // lane r (and r + 32) holds rank r's slice of this bin
     int lo[2], hi[2];
 #pragma unroll
@@ -1191,18 +1194,31 @@ densify_kernel(const __grid_constant__ Lists lists, int n, int logn, int log_w, 
       }
     }
     __syncwarp();
-    for (int r = 0; r < n; ++r) {
-      const int a = __shfl_sync(0xffffffffu, r < 32 ? lo[0] : lo[1], r & 31);
-      const int e = __shfl_sync(0xffffffffu, r < 32 ? hi[0] : hi[1], r & 31);
-      const int32_t* ip = lists.idx[r];
-      for (int j = a + lane; j < e; j += 32) {
-        const uint32_t slot = (uint32_t)__ldg(ip + j) - base;
-        if (slot < (uint32_t)W) atomicOr(&mk[slot], 1ull << r);
-      }
+    // Rank by rank in chunks of up to 32 entries (walk_bin, 8 chunks' loads
+    // in flight): a list is strictly ascending, so the lanes of one chunk
+    // hold distinct keys and a plain read-modify-write of the mask is
+    // race-free; chunks are ordered by a warp barrier.
+    BinRows R;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      R.lo[h] = lo[h];
+      R.len[h] = hi[h] - lo[h];
     }
+    int key[kDensChunks], rk[kDensChunks];
+    walk_bin<kDensChunks>(
+        R, n,
+        [&](int t, int r, int pos) {
+          key[t] = __ldg(lists.idx[r] + pos);
+          rk[t] = r;
+        },
+        [&](int t, bool ok) {
+          const uint32_t slot = (uint32_t)key[t] - base;
+          if (ok && slot < (uint32_t)W) mk[slot] |= 1ull << rk[t];
+        });
     __syncwarp();
     for (int i = lane; i < W; i += 32) {
       unsigned long long m = mk[i];
+      mk[i] = 0ull;
       if (m) {
 #pragma unroll
         for (int level = 1; level <= 6; ++level) {
