@@ -1157,27 +1157,39 @@ part_write_kernel(const int32_t* idx, const float* val, int64_t nnz, int64_t til
 constexpr int kDensWarps = 4;
 constexpr int kDensChunks = 8;
 
-__device__ __forceinline__ unsigned long long group_sel(int level) {
+// Bits 0, 2^L, 2 * 2^L, ... of a holder mask: the first rank of every group
+// of 2^L consecutive ranks.
+template <typename M>
+__device__ __forceinline__ M group_sel(int level) {
   switch (level) {
-    case 1: return 0x5555555555555555ull;
-    case 2: return 0x1111111111111111ull;
-    case 3: return 0x0101010101010101ull;
-    case 4: return 0x0001000100010001ull;
-    case 5: return 0x0000000100000001ull;
-    default: return 0x1ull;
+    case 1: return (M)0x5555555555555555ull;
+    case 2: return (M)0x1111111111111111ull;
+    case 3: return (M)0x0101010101010101ull;
+    case 4: return (M)0x0001000100010001ull;
+    case 5: return (M)0x0000000100000001ull;
+    default: return (M)1;
   }
 }
 
+__device__ __forceinline__ int popc_mask(uint32_t m) { return __popc(m); }
+__device__ __forceinline__ int popc_mask(unsigned long long m) { return __popcll(m); }
+
+// M: the holder mask type (32-bit up to 32 ranks, else 64-bit); kLogN:
+// log2 of the rank count.  Per warp: masks mk[W] and the list of the bin's
+// keys in first-holder order, mlist[W] (u16).
+template <typename M, int kLogN>
 __global__ void __launch_bounds__(kDensWarps * 32)
-densify_kernel(const __grid_constant__ Lists lists, int n, int logn, int log_w, int bins,
+densify_kernel(const __grid_constant__ Lists lists, int n, int log_w, int bins,
                const int32_t* starts, int64_t total_nnz, unsigned long long* counts) {
-  extern __shared__ unsigned long long masks_all[];
+  extern __shared__ __align__(16) unsigned char dens_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int W = 1 << log_w;
-  unsigned long long* mk = masks_all + (size_t)warp * W;
-  unsigned long long cnt[6] = {0, 0, 0, 0, 0, 0};
+  M* mk = reinterpret_cast<M*>(dens_smem + (size_t)warp * W * (sizeof(M) + 2));
+  uint16_t* mlist = reinterpret_cast<uint16_t*>(mk + W);
+  const unsigned lt = lanemask_lt();
+  unsigned long long cnt[kLogN > 0 ? kLogN : 1] = {};
   const int nwarps = gridDim.x * kDensWarps;
-  for (int i = lane; i < W; i += 32) mk[i] = 0ull;  // then cleared as it is read
+  for (int i = lane; i < W; i += 32) mk[i] = 0;  // then cleared as it is read
   for (int b = blockIdx.x * kDensWarps + warp; b < bins; b += nwarps) {
     const uint32_t base = (uint32_t)b << log_w;
     // lane r (and r + 32) holds rank r's slice of this bin
@@ -1197,7 +1209,8 @@ densify_kernel(const __grid_constant__ Lists lists, int n, int logn, int log_w, 
     // Rank by rank in chunks of up to 32 entries (walk_bin, 8 chunks' loads
     // in flight): a list is strictly ascending, so the lanes of one chunk
     // hold distinct keys and a plain read-modify-write of the mask is
-    // race-free; chunks are ordered by a warp barrier.
+    // race-free; chunks are ordered by a warp barrier.  A key whose mask was
+    // empty joins the member list.
     BinRows R;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -1205,6 +1218,7 @@ densify_kernel(const __grid_constant__ Lists lists, int n, int logn, int log_w, 
       R.len[h] = hi[h] - lo[h];
     }
     int key[kDensChunks], rk[kDensChunks];
+    int members = 0;
     walk_bin<kDensChunks>(
         R, n,
         [&](int t, int r, int pos) {
@@ -1213,29 +1227,35 @@ densify_kernel(const __grid_constant__ Lists lists, int n, int logn, int log_w, 
         },
         [&](int t, bool ok) {
           const uint32_t slot = (uint32_t)key[t] - base;
-          if (ok && slot < (uint32_t)W) mk[slot] |= 1ull << rk[t];
+          bool first = false;
+          if (ok && slot < (uint32_t)W) {
+            const M old = mk[slot];
+            mk[slot] = old | ((M)1 << rk[t]);
+            first = old == 0;
+          }
+          const unsigned fresh = __ballot_sync(0xffffffffu, first);
+          if (first) mlist[members + __popc(fresh & lt)] = (uint16_t)slot;
+          members += __popc(fresh);
         });
     __syncwarp();
-    for (int i = lane; i < W; i += 32) {
-      unsigned long long m = mk[i];
-      mk[i] = 0ull;
-      if (m) {
+    // every member: fold its mask level by level and count the groups
+    for (int j = lane; j < members; j += 32) {
+      const int slot = mlist[j];
+      M m = mk[slot];
+      mk[slot] = 0;
 #pragma unroll
-        for (int level = 1; level <= 6; ++level) {
-          if (level <= logn) {
-            m |= m >> (1 << (level - 1));
-            cnt[level - 1] += __popcll(m & group_sel(level));
-          }
-        }
+      for (int level = 1; level <= kLogN; ++level) {
+        m |= m >> (1 << (level - 1));
+        cnt[level - 1] += popc_mask((M)(m & group_sel<M>(level)));
       }
     }
     __syncwarp();
   }
 #pragma unroll
-  for (int level = 1; level <= 6; ++level) {
+  for (int level = 1; level <= kLogN; ++level) {
     unsigned long long v = cnt[level - 1];
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0 && level <= logn && v) atomicAdd(&counts[level], v);
+    if (lane == 0 && v) atomicAdd(&counts[level], v);
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(&counts[0], (unsigned long long)total_nnz);
 }
@@ -1390,6 +1410,20 @@ zr_status sparse_launch(const int32_t* const* idx, const float* const* val, cons
   return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
 }
 
+// The densification kernel for the rank count: 32-bit masks up to 32 ranks
+// (log2 n <= 5), 64-bit masks above (log2 n = 6).
+const void* densify_fn(bool wide, int logn) {
+  if (wide) return (const void*)densify_kernel<unsigned long long, 6>;
+  switch (logn) {
+    case 0: return (const void*)densify_kernel<uint32_t, 0>;
+    case 1: return (const void*)densify_kernel<uint32_t, 1>;
+    case 2: return (const void*)densify_kernel<uint32_t, 2>;
+    case 3: return (const void*)densify_kernel<uint32_t, 3>;
+    case 4: return (const void*)densify_kernel<uint32_t, 4>;
+    default: return (const void*)densify_kernel<uint32_t, 5>;
+  }
+}
+
 // Densification workspace: [status] then the bin starts (the sparse
 // layout's first region, with no partitions).
 size_t densify_workspace_bytes(int n, int64_t dense_size) {
@@ -1431,22 +1465,30 @@ zr_status densify_launch(const int32_t* const* idx, const int64_t* nnz, int n, i
     bin_starts_kernel<<<dim3((unsigned)gx, (unsigned)n), 256, 0, stream>>>(
         lists, (int)dense_size, g.log_w, bins, starts, status);
   }
-  const size_t smem = (size_t)kDensWarps * ((size_t)1 << g.log_w) * 8;
+  const bool wide = n > 32;
+  const size_t per_key = (wide ? 8 : 4) + 2;  // mask + member list entry
+  const size_t smem = (size_t)kDensWarps * ((size_t)1 << g.log_w) * per_key;
+  const void* fn = densify_fn(wide, logn);
   static bool attr_set[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ZR_ERR_CUDA;
   if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(densify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)((size_t)kDensWarps * 4096 * 8)) != cudaSuccess)
-      return ZR_ERR_CUDA;
+    for (int lg = 0; lg <= 5; ++lg)
+      for (int wd = 0; wd < 2; ++wd)
+        if (cudaFuncSetAttribute(densify_fn(wd == 1, lg),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)((size_t)kDensWarps * 4096 * (wd ? 10 : 6))) != cudaSuccess)
+          return ZR_ERR_CUDA;
     attr_set[dev] = true;
   }
   const int64_t units = (g.bins + kDensWarps - 1) / kDensWarps;
-  densify_kernel<<<(unsigned)grid_for(units, per_sm((const void*)densify_kernel, kDensWarps * 32,
-                                                      smem)),
-                   kDensWarps * 32, smem, stream>>>(lists, n, logn, g.log_w, bins, starts,
-                                                     total_nnz,
-                                                     reinterpret_cast<unsigned long long*>(d_union_counts));
+  const unsigned grid = (unsigned)grid_for(units, per_sm(fn, kDensWarps * 32, smem));
+  int log_w = g.log_w;
+  unsigned long long* counts = reinterpret_cast<unsigned long long*>(d_union_counts);
+  void* args[] = {(void*)&lists, (void*)&n, (void*)&log_w, (void*)&bins, (void*)&starts,
+                  (void*)&total_nnz, (void*)&counts};
+  if (cudaLaunchKernel(fn, dim3(grid), dim3(kDensWarps * 32), args, smem, stream) != cudaSuccess)
+    return ZR_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
 }
 

@@ -25,7 +25,7 @@ def run(torch, zr, lists, m):
     return [int(v) for v in counts.cpu().numpy()]
 
 
-@pytest.mark.parametrize("n", [1, 2, 4, 8, 16, 64])
+@pytest.mark.parametrize("n", [1, 2, 4, 8, 16, 32, 64])
 def test_random_lists(env, n):
     torch, zr = env
     rng = np.random.default_rng(n)
