@@ -66,13 +66,19 @@ struct BucketParams {
 
 constexpr int kThreads = 128;
 // Default shape: kBatch ranks' loads issued back to back before folding,
-// kUnroll vectors per thread per pass.  Folds of at most 4 ranks take 4
-// vectors per thread (4 ranks per batch) instead, so that a thread still
-// keeps 256 bytes of loads in flight.
+// kUnroll vectors per thread per pass.  Smaller folds take more vectors per
+// thread, so that a thread still keeps about 256 bytes of loads in flight:
+// at most 2 ranks 8 vectors, at most 4 ranks 4 vectors, 5 or 6 ranks 3.
 constexpr int kBatch = 8;
 constexpr int kUnroll = 2;
+constexpr int kTinyFold = 2;
+constexpr int kTinyBatch = 2;
+constexpr int kTinyUnroll = 8;
 constexpr int kSmallBatch = 4;
 constexpr int kSmallUnroll = 4;
+constexpr int kMediumFold = 6;
+constexpr int kMediumBatch = 6;
+constexpr int kMediumUnroll = 3;
 
 template <typename T>
 struct Elem;
@@ -312,15 +318,24 @@ RingJob make_job(int n, int64_t m, int k, int mode, uint64_t seed, uint64_t step
 
 template <typename T>
 zr_status launch_one(RingParams& P, cudaStream_t stream) {
-  const bool small = P.job.n - P.job.k <= kSmallBatch;
-  P.job.bps = blocks_per_slice<T>(P.job.chunk, small ? kSmallUnroll : kUnroll);
+  const int fold = P.job.n - P.job.k;  // ranks folded per element
+  const int shape = fold <= kTinyFold      ? 0
+                    : fold <= kSmallBatch  ? 1
+                    : fold <= kMediumFold  ? 2
+                                           : 3;
+  const int unroll[4] = {kTinyUnroll, kSmallUnroll, kMediumUnroll, kUnroll};
+  P.job.bps = blocks_per_slice<T>(P.job.chunk, unroll[shape]);
   dim3 grid((unsigned)P.job.bps, (unsigned)P.job.n);
-  if (P.job.drop_thr != 0) {
-    if (small) ring_fused_kernel<T, true, kSmallUnroll, kSmallBatch><<<grid, kThreads, 0, stream>>>(P);
-    else ring_fused_kernel<T, true><<<grid, kThreads, 0, stream>>>(P);
-  } else {
-    if (small) ring_fused_kernel<T, false, kSmallUnroll, kSmallBatch><<<grid, kThreads, 0, stream>>>(P);
-    else ring_fused_kernel<T, false><<<grid, kThreads, 0, stream>>>(P);
+  const bool drop = P.job.drop_thr != 0;
+  switch (shape * 2 + (drop ? 1 : 0)) {
+    case 0: ring_fused_kernel<T, false, kTinyUnroll, kTinyBatch><<<grid, kThreads, 0, stream>>>(P); break;
+    case 1: ring_fused_kernel<T, true, kTinyUnroll, kTinyBatch><<<grid, kThreads, 0, stream>>>(P); break;
+    case 2: ring_fused_kernel<T, false, kSmallUnroll, kSmallBatch><<<grid, kThreads, 0, stream>>>(P); break;
+    case 3: ring_fused_kernel<T, true, kSmallUnroll, kSmallBatch><<<grid, kThreads, 0, stream>>>(P); break;
+    case 4: ring_fused_kernel<T, false, kMediumUnroll, kMediumBatch><<<grid, kThreads, 0, stream>>>(P); break;
+    case 5: ring_fused_kernel<T, true, kMediumUnroll, kMediumBatch><<<grid, kThreads, 0, stream>>>(P); break;
+    case 6: ring_fused_kernel<T, false><<<grid, kThreads, 0, stream>>>(P); break;
+    default: ring_fused_kernel<T, true><<<grid, kThreads, 0, stream>>>(P); break;
   }
   return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
 }
