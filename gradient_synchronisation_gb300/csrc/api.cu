@@ -7,6 +7,7 @@
 
 #include <algorithm>
 #include <utility>
+#include <atomic>
 #include <vector>
 
 #include "zr.h"
@@ -15,14 +16,15 @@
 namespace zr {
 
 int sm_count() {
-  static int cached[64];
+  static std::atomic<int> cached[64];  // 0 until first asked; any thread may fill it
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cached[dev] > 0) return cached[dev];
+  const int c = cached[dev].load(std::memory_order_relaxed);
+  if (c > 0) return c;
   int s = 0;
   if (cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || s <= 0)
     s = 148;
-  cached[dev] = s;
+  cached[dev].store(s, std::memory_order_relaxed);
   return s;
 }
 

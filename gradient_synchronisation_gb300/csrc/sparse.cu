@@ -39,6 +39,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "zr.h"
 #include "zr_device.cuh"
 #include "zr_internal.h"
@@ -1299,17 +1302,22 @@ size_t write_smem(int place, int log_w, int parts) {
 // Per-device cached occupancy, and the dynamic shared-memory opt-in of the
 // write kernels (done once per device).
 struct DeviceInfo {
-  int ready = 0;
+  std::atomic<int> ready{0};
   int count_per_sm = 1;
   int part_count_per_sm = 1;
 };
 
+// One thread fills a device's entry (under the lock); later calls read it
+// after seeing `ready`.
 DeviceInfo* device_info() {
   static DeviceInfo info[64];
+  static std::mutex init_lock;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   DeviceInfo& d = info[dev];
-  if (!d.ready) {
+  if (d.ready.load(std::memory_order_acquire)) return &d;
+  std::lock_guard<std::mutex> guard(init_lock);
+  if (!d.ready.load(std::memory_order_relaxed)) {
     for (int place = 0; place < 3; ++place) {
       const int most = (int)write_smem(place, 12, place == kPlaceSort ? ZR_MAX_PARTS : 32);
       for (int a = 0; a < 3; ++a)
@@ -1320,7 +1328,7 @@ DeviceInfo* device_info() {
     }
     d.count_per_sm = per_sm((const void*)bin_count_kernel, kBinThreads, 0);
     d.part_count_per_sm = per_sm((const void*)part_count_kernel<false, 3>, kPartThreads, 0);
-    d.ready = 1;
+    d.ready.store(1, std::memory_order_release);
   }
   return &d;
 }
@@ -1469,17 +1477,19 @@ zr_status densify_launch(const int32_t* const* idx, const int64_t* nnz, int n, i
   const size_t per_key = (wide ? 8 : 4) + 2;  // mask + member list entry
   const size_t smem = (size_t)kDensWarps * ((size_t)1 << g.log_w) * per_key;
   const void* fn = densify_fn(wide, logn);
-  static bool attr_set[64];
+  static std::atomic<bool> attr_set[64];
+  static std::mutex attr_lock;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ZR_ERR_CUDA;
-  if (!attr_set[dev]) {
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> guard(attr_lock);
     for (int lg = 0; lg <= 5; ++lg)
       for (int wd = 0; wd < 2; ++wd)
         if (cudaFuncSetAttribute(densify_fn(wd == 1, lg),
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)((size_t)kDensWarps * 4096 * (wd ? 10 : 6))) != cudaSuccess)
           return ZR_ERR_CUDA;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   const int64_t units = (g.bins + kDensWarps - 1) / kDensWarps;
   const unsigned grid = (unsigned)grid_for(units, per_sm(fn, kDensWarps * 32, smem));
