@@ -20,9 +20,10 @@
 //      bin's first output position in that partition.
 //   4. write:   per bin, a warp walks the bin rank by rank in chunks of up
 //      to 32 consecutive entries of one rank (the loads of 8 chunks in
-//      flight; one ballot gives each chunk's rank) and folds them into a
-//      warp-private W-float window in ascending rank order, which is the
-//      left fold of the holders' values.  Then the members are placed into
+//      flight; one ballot gives each chunk's rank), or, where bins hold few
+//      entries, flattened in groups of 32 across rank boundaries applied in
+//      ascending runs, and folds them into a warp-private W-float window in
+//      ascending rank order, which is the left fold of the holders' values.  Then the members are placed into
 //      their partitions' runs: through per-lane partition counters where
 //      bins hold few entries, partition by partition from per-partition
 //      member bitmaps where they hold many, and by a counting sort above 32
@@ -658,6 +659,7 @@ bin_write_kernel(const __grid_constant__ Lists lists, int n, int log_w, int bins
                  int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ long long offs[ZR_MAX_PARTS + 1];
+  __shared__ BinRanks flat_all[kPlace == kPlaceLane ? kWriteWarps : 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int W = 1 << log_w;
   const int words = W >> 5;
@@ -712,6 +714,7 @@ bin_write_kernel(const __grid_constant__ Lists lists, int n, int log_w, int bins
   for (; b < bins; b += nwarps) {
     const uint32_t base = (uint32_t)b << log_w;
     const BinRows R = bin_rows(lists, n, fetch);
+    const BinFetch fetch_cur = fetch;
     const int pc = pc_next;
     const long long pe = pe_next;
     if (b + nwarps < bins) {
@@ -726,21 +729,61 @@ bin_write_kernel(const __grid_constant__ Lists lists, int n, int log_w, int bins
     __syncwarp();
 
     // fold
-    int key[kWriteChunks];
-    float val[kWriteChunks];
-    walk_bin<kWriteChunks>(
-        R, n,
-        [&](int t, int r, int pos) {
-          key[t] = __ldg(lists.idx[r] + pos);
-          val[t] = __ldg(lists.val[r] + pos);
-        },
-        [&](int t, bool ok) {
-          const uint32_t slot = (uint32_t)key[t] - base;
-          if (ok && slot < (uint32_t)W) {
-            acc[slot] = __fadd_rn(acc[slot], val[t]);
-            atomicOr(&ub[slot >> 5], 1u << (slot & 31));
-          }
-        });
+    if (kLane) {
+      // Sparse bins: the flattened walk (groups of 32 entries across rank
+      // boundaries).  Keys that strictly ascend across a group's lanes are
+      // distinct and apply at once; otherwise each maximal ascending run of
+      // lanes goes in lane order, so a key held by two ranks meets the lower
+      // rank first.
+      BinRanks& F = flat_all[warp];
+      const int total = bin_commit(lists, n, fetch_cur, F);
+      int fkey[kBatch];
+      float fval[kBatch];
+      for_bin_entries(
+          lists, n, F, total, status,
+          [&](int t, int r, int pos) {
+            fkey[t] = __ldg(lists.idx[r] + pos);
+            fval[t] = __ldg(lists.val[r] + pos);
+          },
+          [&](int k0, const int (&rank)[kBatch]) {
+#pragma unroll
+            for (int t = 0; t < kBatch; ++t) {
+              if (k0 + 32 * t < total) {
+                const uint32_t slot = (uint32_t)fkey[t] - base;
+                const bool live = rank[t] >= 0;
+                const bool in = live && slot < (uint32_t)W;
+                const int prev = __shfl_up_sync(0xffffffffu, fkey[t], 1);
+                const unsigned desc =
+                    __ballot_sync(0xffffffffu, live && lane > 0 && prev >= fkey[t]);
+                const int run_id = __popc(desc & (lt | (1u << lane)));
+                const int runs = __popc(desc) + 1;
+                for (int q = 0; q < runs; ++q) {
+                  if (in && run_id == q) {
+                    acc[slot] = __fadd_rn(acc[slot], fval[t]);
+                    atomicOr(&ub[slot >> 5], 1u << (slot & 31));
+                  }
+                  __syncwarp();
+                }
+              }
+            }
+          });
+    } else {
+      int key[kWriteChunks];
+      float val[kWriteChunks];
+      walk_bin<kWriteChunks>(
+          R, n,
+          [&](int t, int r, int pos) {
+            key[t] = __ldg(lists.idx[r] + pos);
+            val[t] = __ldg(lists.val[r] + pos);
+          },
+          [&](int t, bool ok) {
+            const uint32_t slot = (uint32_t)key[t] - base;
+            if (ok && slot < (uint32_t)W) {
+              acc[slot] = __fadd_rn(acc[slot], val[t]);
+              atomicOr(&ub[slot >> 5], 1u << (slot & 31));
+            }
+          });
+    }
 
     if (kLane) {
       uint32_t* row = rows + lane * rs;
