@@ -56,8 +56,8 @@ TRAFFIC = {
 # Kernel launches each library call makes (counted from the library source).
 # Kernels of this library launched per component per step (the status-word
 # memset of the sparse path is a runtime memset, not counted).
-LAUNCHES = {"ring": 1, "skip": 1, "sparse": 5, "partition": 3, "dropout": 1, "buckets": 1,
-            "hb_encode": 3, "hb_decode": 3, "hb_sets": 4, "densify": 2}
+LAUNCHES = {"ring": 1, "skip": 1, "rs_only": 1, "sparse": 5, "partition": 3, "dropout": 1,
+            "buckets": 1, "hb_encode": 3, "hb_decode": 3, "hb_sets": 4, "densify": 2}
 
 
 def torch_stream(torch):
@@ -72,9 +72,8 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=("ring", "skip", "sparse", "partition", "dropout", "buckets",
-                                       "densify",
-                                       "hb_encode", "hb_decode", "hb_sets"),
+    ap.add_argument("--only", choices=("ring", "skip", "rs_only", "sparse", "partition", "dropout",
+                                       "buckets", "densify", "hb_encode", "hb_decode", "hb_sets"),
                     default=None,
                     help="profiling: time one component alone (prints a profiling line, not the "
                          "benchmark line)")
@@ -206,7 +205,8 @@ class Workload:
         self.n, self.k = c2["n"], c2["skip_k"]
         self.m = dense_m or c2["m"]
         self.seed = c2["skip_seed"]
-        self.dense_on = any(c in self.components for c in ("ring", "skip", "dropout", "buckets"))
+        self.dense_on = any(c in self.components
+                            for c in ("ring", "skip", "rs_only", "dropout", "buckets"))
         self.sparse_on = any(c in self.components
                              for c in ("sparse", "partition", "hb_encode", "hb_decode", "hb_sets",
                                        "densify"))
@@ -274,6 +274,9 @@ class Workload:
         if self.dense_on:
             out["ring"] = 2 * self.n * self.m * s
             out["skip"] = (self.n - self.k) * self.m * s + self.n * self.m * s
+            # Reduce-Scatter only: the folded ranks read, each slice written
+            # once, to its holder
+            out["rs_only"] = (self.n - self.k) * self.m * s + self.m * s
             out["dropout"] = 2 * self.n * self.m * s
             out["buckets"] = sum((self.n - b["k"]) * b["m"] * s + self.n * b["m"] * s
                                  for b in self.buckets)
@@ -297,6 +300,9 @@ class Workload:
             zr.ring_allreduce(self.bufs, average=True)
         elif name == "skip":
             zr.skipreduce(self.bufs, k=self.k, mode=zr.ZR_SKIP_RANDOM, seed=self.seed, step=i)
+        elif name == "rs_only":
+            zr.skipreduce(self.bufs, k=self.k, mode=zr.ZR_SKIP_RANDOM, seed=self.seed, step=i,
+                          rs_only=True)
         elif name == "dropout":
             zr.allreduce_dropout(self.bufs, 0.5, seed=self.seed, step=i)
         elif name == "buckets":
@@ -330,7 +336,7 @@ class Workload:
                 events[name].record()
 
 
-DENSE_PARTS = ("ring", "skip", "dropout", "buckets")
+DENSE_PARTS = ("ring", "skip", "rs_only", "dropout", "buckets")
 
 
 def timed_overlap(torch, W, steps, warmup):
