@@ -56,7 +56,9 @@ def test_random_small(env, n):
         idx_l, val_l = workloads.random_coo(n, m, nnz, seed=n * 7 + m, shared=min(shared, nnz))
         for n_parts in (0, 1, 8, 256):
             check(torch, zr, idx_l, val_l, m, n_parts, seed=n_parts)
+        # the 1/N average on the per-lane and the sort placements
         check(torch, zr, idx_l, val_l, m, 8, seed=5, average=True)
+        check(torch, zr, idx_l, val_l, m, 256, seed=6, average=True)
 
 
 def test_edge_cases(env):
