@@ -53,7 +53,7 @@ namespace {
 constexpr int kBinWarps = 8;             // warps per CTA in the count and write kernels
 constexpr int kBinThreads = kBinWarps * 32;
 constexpr int kStartsUnroll = 4;         // starts kernel: groups of 4 keys per thread per step
-constexpr int kBatch = 8;                // count pass: groups of 32 entries per load batch
+constexpr int kBatch = 4;                // flattened walk: groups of 32 entries per load batch (2-12 measured)
 constexpr int kWriteWarps = 4;           // warps per CTA in the write kernel
 constexpr int kWriteThreads = kWriteWarps * 32;
 constexpr int kPartTile = 1024;          // zr_partition: entries per tile
