@@ -57,7 +57,7 @@ EXPORTS = (
     "zr_version", "zr_partition_static", "zr_skipreduce_buckets", "zr_allreduce_dropout",
     "zr_hash_index_sets", "zr_hash_bitmap_encode", "zr_hash_bitmap_decode",
     "zr_hash_bitmap_workspace_size", "zr_densification", "zr_densification_workspace_size",
-    "zr_choose_scheme",
+    "zr_choose_scheme", "zr_test_barrier_skip",
 )
 ZR_SCHEME_BALANCED = 0
 ZR_SCHEME_HIERARCHICAL = 1
@@ -109,6 +109,7 @@ def _load():
         "zr_hash_bitmap_workspace_size": (sz, [i64, i32]),
         "zr_densification": (i32, [PP, ctypes.POINTER(i64), i32, i64, P, P, sz, P]),
         "zr_densification_workspace_size": (sz, [i32, i64]),
+        "zr_test_barrier_skip": (None, [i32]),
         "zr_choose_scheme": (i32, [ctypes.POINTER(i64), i32, ctypes.POINTER(ctypes.c_double),
                                    ctypes.POINTER(ctypes.c_double),
                                    ctypes.POINTER(ctypes.c_double)]),
@@ -218,6 +219,11 @@ def zr_sparse_aggregate(idx, val, nnz, n, dense_size, n_parts, part_seed, averag
 
 def zr_sparse_workspace_size(n, dense_size, n_parts):
     return lib().zr_sparse_workspace_size(n, dense_size, n_parts)
+
+
+def zr_test_barrier_skip(cta):
+    """Testing only: the CTA ``cta`` skips its grid-wait arrival (-1: off)."""
+    lib().zr_test_barrier_skip(cta)
 
 
 def zr_partition(idx, val, nnz, n_parts, part_seed, out_idx, out_val, d_offsets, ws, ws_bytes,

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libzr.so")
-SOURCES = ["api.cu", "ring.cu", "sparse.cu", "noalloc.cu", "hashbitmap.cu"]
+SOURCES = ["api.cu", "ring.cu", "sparse.cu", "partition.cu", "noalloc.cu", "hashbitmap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-I", INCLUDE, "-I", CSRC]

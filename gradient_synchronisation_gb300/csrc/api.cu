@@ -1,5 +1,5 @@
 // libzr C ABI: argument validation, status mapping and dispatch to the
-// kernels in ring.cu and sparse.cu.  Every check here runs on the host before
+// kernels in ring.cu, sparse.cu, partition.cu and hashbitmap.cu.  Every check here runs on the host before
 // anything is enqueued; a failed check returns without touching any buffer.
 
 #include <cuda_runtime.h>

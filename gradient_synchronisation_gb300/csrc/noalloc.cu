@@ -12,17 +12,25 @@
 // array compiled into the library instead.
 //
 // The scratch is a file-scope __device__ array of ZR_STATIC_SCRATCH_BYTES
-// (every GPU that loads the library holds it until the process exits).  Host
-// code must not hand the array's name to a kernel: on the host that name is
-// only a stand-in symbol.  Its device address is looked up once per device,
-// on the first call made with that device current, with
-// cudaGetSymbolAddress; that first call should therefore come before any
-// stream capture.  Every call on a device shares the one array and clears the
-// parts that must start at zero itself, so calls whose work overlaps on the
-// GPU (different streams without ordering between them) race on it.
+// (every GPU that loads the library holds it until the process exits).  It
+// holds the partition's per-(partition, CTA) count table and the status and
+// grid-wait words, whose size does not depend on the list length, so every
+// valid request fits.  Host code must not hand the array's name to a
+// kernel: on the host that name is only a stand-in symbol.  Its device
+// address is looked up once per device, on the first call made with that
+// device current, with cudaGetSymbolAddress; that first call should
+// therefore come before any stream capture.  The address is kept for the
+// life of the process, so the entry point must not be used on a device after
+// cudaDeviceReset (which reloads the module and can move the array).  Every
+// call on a device shares the one array and clears the parts that must start
+// at zero itself, so calls whose work overlaps on the GPU (different streams
+// without ordering between them) race on it.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <atomic>
+#include <mutex>
 
 #include "zr.h"
 #include "zr_internal.h"
@@ -31,18 +39,25 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_partition_scratch[ZR_STATIC_SCRATCH_BYTES];
 
-// Device address of g_partition_scratch, per device (0 until looked up).
-void* g_scratch_address[64];
+// Device address of g_partition_scratch, per device: null until the first
+// call on that device looks it up (under the lock); read without the lock
+// once set.
+std::atomic<void*> g_scratch_address[64];
+std::mutex g_scratch_lock;
 
 zr_status scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ZR_ERR_CUDA;
-  if (!g_scratch_address[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_partition_scratch) != cudaSuccess || !p) return ZR_ERR_CUDA;
-    g_scratch_address[dev] = p;
+  void* p = g_scratch_address[dev].load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> guard(g_scratch_lock);
+    p = g_scratch_address[dev].load(std::memory_order_relaxed);
+    if (!p) {
+      if (cudaGetSymbolAddress(&p, g_partition_scratch) != cudaSuccess || !p) return ZR_ERR_CUDA;
+      g_scratch_address[dev].store(p, std::memory_order_release);
+    }
   }
-  *out = g_scratch_address[dev];
+  *out = p;
   return ZR_OK;
 }
 

@@ -56,8 +56,6 @@ constexpr int kStartsUnroll = 4;         // starts kernel: groups of 4 keys per 
 constexpr int kBatch = 4;                // flattened walk: groups of 32 entries per load batch (2-12 measured)
 constexpr int kWriteWarps = 4;           // warps per CTA in the write kernel
 constexpr int kWriteThreads = kWriteWarps * 32;
-constexpr int kPartTile = 1024;          // zr_partition: entries per tile
-constexpr int kPartThreads = 256;
 
 struct Lists {
   const int32_t* idx[ZR_MAX_RANKS];
@@ -977,219 +975,6 @@ bin_write_kernel(const __grid_constant__ Lists lists, int n, int log_w, int bins
   }
 }
 
-// ------------------------------------------------------------ partition
-// A stable split of one list by h0, tile by tile (kPartTile entries): a
-// count pass writes every tile's count per partition, the two scan kernels
-// of the union path turn them into each tile's first output position per
-// partition (and the partition totals), and a write pass places the tile's
-// entries.  No CTA waits for another and no counter is shared.
-// Workspace: [unused | totals | chunk totals | tile counts | tile prefixes]
-// (the partition path reports no device-side errors, so it has no status
-// word).
-struct PartLayout {
-  size_t tot, ctot, cnt, excl, total;
-};
-
-PartLayout part_layout(int64_t tiles, int parts) {
-  PartLayout L;
-  const int64_t chunks = (tiles + kChunkBins - 1) >> kChunkLog;
-  L.tot = 256;
-  L.ctot = L.tot + align256((size_t)parts * 8);
-  L.cnt = L.ctot + align256((size_t)chunks * parts * 8);
-  L.excl = L.cnt + align256((size_t)tiles * parts * 4);
-  L.total = L.excl + align256((size_t)tiles * parts * 8);
-  return L;
-}
-
-// kIdentity: the input is the index range itself (position i holds index i,
-// no values) -- the partition that builds Zen's index sets I_p.
-//
-// Up to 32 partitions (kBallot) a warp splits 32 entries at a time with
-// ceil(log2 P) ballots of the partition bits: lane l learns which lanes share
-// its partition (its rank among them) and lane q how many entries of the 32
-// fall in partition q, so counts stay in registers; above 32 partitions a
-// match_any groups the lanes of one partition.
-
-// Lanes whose partition equals the lane index q (kBits partition bits): the
-// AND over the bits of the matching ballots, restricted to live lanes.
-template <int kBits>
-__device__ __forceinline__ unsigned part_lanes(unsigned live_mask, int p, int q) {
-  unsigned m = live_mask;
-#pragma unroll
-  for (int i = 0; i < kBits; ++i) {
-    const unsigned bi = __ballot_sync(0xffffffffu, (p >> i) & 1);
-    m &= ((q >> i) & 1) ? bi : ~bi;
-  }
-  return m;
-}
-
-// Both masks of one step: lanes in the caller's own partition p (same) and
-// lanes in partition q = the lane index (mine_q), from one set of ballots.
-template <int kBits>
-__device__ __forceinline__ void part_masks(unsigned live_mask, int p, unsigned& same,
-                                           unsigned& mine_q) {
-  const int q = threadIdx.x & 31;
-  same = live_mask;
-  mine_q = live_mask;
-#pragma unroll
-  for (int i = 0; i < kBits; ++i) {
-    const unsigned bi = __ballot_sync(0xffffffffu, (p >> i) & 1);
-    same &= ((p >> i) & 1) ? bi : ~bi;
-    mine_q &= ((q >> i) & 1) ? bi : ~bi;
-  }
-}
-
-// kBits: the partitions' bit count when at most 32 (ballots), -1 above
-// (match_any).
-template <bool kIdentity, int kBits>
-__global__ void __launch_bounds__(kPartThreads)
-part_count_kernel(const int32_t* idx, int64_t nnz, int64_t tiles, H0 h, int parts,
-                  int32_t* cnt_g) {
-  constexpr int kPW = kPartThreads / 32;
-  constexpr int kPerWarp = kPartTile / kPW;
-  __shared__ int32_t cnt[ZR_MAX_PARTS];
-  __shared__ int32_t wcnt[kPW][32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const H0 hash = h;
-  constexpr bool kBallot = kBits >= 0;
-  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-    const int64_t hi = min(t * kPartTile + kPartTile, nnz);
-    if (kBallot) {
-      const int64_t lo = t * kPartTile + (int64_t)warp * kPerWarp;
-      int c = 0;  // lane q: entries of partition q among the warp's
-#pragma unroll
-      for (int j = 0; j < kPerWarp; j += 32) {
-        const int64_t i = lo + j + lane;
-        const bool live = i < hi;
-        const int p = live ? (int)hash(kIdentity ? (uint32_t)i : (uint32_t)idx[i]) : 0;
-        c += __popc(part_lanes<kBallot ? kBits : 0>(__ballot_sync(0xffffffffu, live), p, lane));
-      }
-      wcnt[warp][lane] = c;
-      __syncthreads();
-      for (int q = tid; q < parts; q += kPartThreads) {
-        int s = 0;
-#pragma unroll
-        for (int w = 0; w < kPW; ++w) s += wcnt[w][q];
-        __stcg(cnt_g + (size_t)q * tiles + t, s);
-      }
-      __syncthreads();
-    } else {
-      for (int q = tid; q < parts; q += kPartThreads) cnt[q] = 0;
-      __syncthreads();
-      for (int64_t i = t * kPartTile + tid; i < t * kPartTile + kPartTile; i += kPartThreads) {
-        const bool live = i < hi;
-        const int p = live ? (int)hash(kIdentity ? (uint32_t)i : (uint32_t)idx[i]) : parts;
-        const unsigned peers = __match_any_sync(0xffffffffu, p);
-        if (live && (peers & lanemask_lt()) == 0) atomicAdd(&cnt[p], __popc(peers));
-      }
-      __syncthreads();
-      for (int q = tid; q < parts; q += kPartThreads)
-        __stcg(cnt_g + (size_t)q * tiles + t, cnt[q]);
-      __syncthreads();
-    }
-  }
-}
-
-// Each warp owns kPartTile / warps consecutive entries of the tile and walks
-// them 32 at a time, so the entries of one partition leave in input order.
-template <bool kIdentity, int kBits>
-__global__ void __launch_bounds__(kPartThreads)
-part_write_kernel(const int32_t* idx, const float* val, int64_t nnz, int64_t tiles, H0 h,
-                  int parts, const long long* excl_g, const long long* tot_g, int32_t* out_idx,
-                  float* out_val, int64_t* d_offsets) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  long long* wbase = reinterpret_cast<long long*>(smem);  // warps * parts
-  __shared__ long long offs[ZR_MAX_PARTS + 1];
-  constexpr int kPW = kPartThreads / 32;
-  constexpr int kPerWarp = kPartTile / kPW;
-  constexpr int kSteps = kPerWarp / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned lt = lanemask_lt();
-  const H0 hash = h;
-  constexpr bool kBallot = kBits >= 0;
-  load_partition_offsets(tot_g, parts, offs, d_offsets, nullptr);
-  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-    const int64_t lo = t * kPartTile + (int64_t)warp * kPerWarp;
-    const int64_t hi = min(t * kPartTile + kPartTile, nnz);
-    if (kBallot) {
-      // the warp's keys and partitions stay in registers between the passes
-      int32_t key[kSteps];
-      int part[kSteps];
-      int c = 0;
-#pragma unroll
-      for (int s = 0; s < kSteps; ++s) {
-        const int64_t i = lo + s * 32 + lane;
-        const bool live = i < hi;
-        key[s] = live ? (kIdentity ? (int32_t)i : idx[i]) : 0;
-        part[s] = live ? (int)hash((uint32_t)key[s]) : 0;
-        c += __popc(
-            part_lanes<kBallot ? kBits : 0>(__ballot_sync(0xffffffffu, live), part[s], lane));
-      }
-      long long* wc = wbase;  // [warp][32] counts, then bases
-      wc[warp * 32 + lane] = c;
-      __syncthreads();
-      // lane q: partition q's first output position for this warp's entries
-      long long run = 0;
-      if (lane < parts) {
-        run = offs[lane] + __ldcg(excl_g + (size_t)lane * tiles + t);
-        for (int w = 0; w < warp; ++w) run += wc[w * 32 + lane];
-      }
-      __syncthreads();
-#pragma unroll
-      for (int s = 0; s < kSteps; ++s) {
-        const int64_t i = lo + s * 32 + lane;
-        const bool live = i < hi;
-        unsigned same, mine_q;
-        part_masks<kBallot ? kBits : 0>(__ballot_sync(0xffffffffu, live), part[s], same, mine_q);
-        const long long at = __shfl_sync(0xffffffffu, run, part[s]);
-        if (live) {
-          const long long dst = at + __popc(same & lt);
-          out_idx[dst] = key[s];
-          if (!kIdentity) out_val[dst] = val[i];
-        }
-        run += __popc(mine_q);
-      }
-    } else {
-      for (int q = threadIdx.x; q < kPW * parts; q += kPartThreads) wbase[q] = 0;
-      __syncthreads();
-      for (int j = 0; j < kPerWarp; j += 32) {
-        const int64_t i = lo + j + lane;
-        const bool live = i < hi;
-        const int p = live ? (int)hash(kIdentity ? (uint32_t)i : (uint32_t)idx[i]) : parts;
-        const unsigned peers = __match_any_sync(0xffffffffu, p);
-        if (live && (peers & lt) == 0) wbase[warp * parts + p] += __popc(peers);
-        __syncwarp();
-      }
-      __syncthreads();
-      for (int q = threadIdx.x; q < parts; q += kPartThreads) {
-        long long run = offs[q] + __ldcg(excl_g + (size_t)q * tiles + t);
-        for (int w = 0; w < kPW; ++w) {
-          const long long c = wbase[w * parts + q];
-          wbase[w * parts + q] = run;
-          run += c;
-        }
-      }
-      __syncthreads();
-      for (int j = 0; j < kPerWarp; j += 32) {
-        const int64_t i = lo + j + lane;
-        const bool live = i < hi;
-        const int32_t key = live ? (kIdentity ? (int32_t)i : idx[i]) : 0;
-        const int p = live ? (int)hash((uint32_t)key) : parts;
-        const unsigned peers = __match_any_sync(0xffffffffu, p);
-        if (live) {
-          const long long dst = wbase[warp * parts + p] + __popc(peers & lt);
-          out_idx[dst] = key;
-          if (!kIdentity) out_val[dst] = val[i];
-        }
-        __syncwarp();
-        if (live && (peers & lt) == 0) wbase[warp * parts + p] += __popc(peers);
-        __syncwarp();
-      }
-    }
-    __syncthreads();
-  }
-}
-
 // ------------------------------------------------------------ densification
 // Union sizes of rank groups (Zen section 2.3, the densification ratios
 // gamma_k of Equations (1) and (2)).  Per bin, a warp ORs 1 << r into a
@@ -1347,7 +1132,6 @@ size_t write_smem(int place, int log_w, int parts) {
 struct DeviceInfo {
   std::atomic<int> ready{0};
   int count_per_sm = 1;
-  int part_count_per_sm = 1;
 };
 
 // One thread fills a device's entry (under the lock); later calls read it
@@ -1370,7 +1154,6 @@ DeviceInfo* device_info() {
           return nullptr;
     }
     d.count_per_sm = per_sm((const void*)bin_count_kernel, kBinThreads, 0);
-    d.part_count_per_sm = per_sm((const void*)part_count_kernel<false, 3>, kPartThreads, 0);
     d.ready.store(1, std::memory_order_release);
   }
   return &d;
@@ -1543,99 +1326,6 @@ zr_status densify_launch(const int32_t* const* idx, const int64_t* nnz, int n, i
   if (cudaLaunchKernel(fn, dim3(grid), dim3(kDensWarps * 32), args, smem, stream) != cudaSuccess)
     return ZR_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
-}
-
-size_t partition_workspace_bytes(int64_t nnz, int n_parts) {
-  const int64_t tiles = (nnz + kPartTile - 1) / kPartTile;
-  return part_layout(tiles, n_parts).total;
-}
-
-namespace {
-// The count (count = true) or write kernel for nbits partition bits (-1:
-// more than 32 partitions).
-template <bool kIdentity, int kB>
-const void* part_kernel_bits(bool count) {
-  return count ? (const void*)part_count_kernel<kIdentity, kB>
-               : (const void*)part_write_kernel<kIdentity, kB>;
-}
-
-template <bool kIdentity>
-const void* part_kernel(bool count, int nbits) {
-  switch (nbits) {
-    case 0: return part_kernel_bits<kIdentity, 0>(count);
-    case 1: return part_kernel_bits<kIdentity, 1>(count);
-    case 2: return part_kernel_bits<kIdentity, 2>(count);
-    case 3: return part_kernel_bits<kIdentity, 3>(count);
-    case 4: return part_kernel_bits<kIdentity, 4>(count);
-    case 5: return part_kernel_bits<kIdentity, 5>(count);
-    default: return part_kernel_bits<kIdentity, -1>(count);
-  }
-}
-
-template <bool kIdentity>
-zr_status partition_run(const int32_t* idx, const float* val, int64_t nnz, int n_parts,
-                        uint64_t part_seed, int32_t* out_idx, float* out_val,
-                        int64_t* d_offsets, void* ws, cudaStream_t stream) {
-  const int64_t tiles = (nnz + kPartTile - 1) / kPartTile;
-  const PartLayout L = part_layout(tiles, n_parts);
-  unsigned char* w = static_cast<unsigned char*>(ws);
-  long long* tot = reinterpret_cast<long long*>(w + L.tot);
-  long long* ctot = reinterpret_cast<long long*>(w + L.ctot);
-  int32_t* cnt = reinterpret_cast<int32_t*>(w + L.cnt);
-  long long* excl = reinterpret_cast<long long*>(w + L.excl);
-  const H0 h = make_h0(part_seed, (uint32_t)n_parts);
-  if (tiles == 0) {
-    if (cudaMemsetAsync(d_offsets, 0, (size_t)(n_parts + 1) * 8, stream) != cudaSuccess)
-      return ZR_ERR_CUDA;
-    return ZR_OK;
-  }
-  if (tiles > 0x7fffffff) return ZR_ERR_UNSUPPORTED;
-  DeviceInfo* dinfo = device_info();
-  if (!dinfo) return ZR_ERR_CUDA;
-  // ballots on ceil(log2 P) partition bits up to 32 partitions, match_any above
-  const int nbits = n_parts > 32 ? -1 : (n_parts > 1 ? 32 - __builtin_clz((unsigned)n_parts - 1) : 0);
-  const bool ballot = nbits >= 0;
-  const unsigned count_grid = (unsigned)grid_for(tiles, dinfo->part_count_per_sm);
-  const void* count_fn = part_kernel<kIdentity>(true, nbits);
-  void* count_args[] = {(void*)&idx, (void*)&nnz, (void*)&tiles, (void*)&h, (void*)&n_parts,
-                        (void*)&cnt};
-  if (cudaLaunchKernel(count_fn, dim3(count_grid), dim3(kPartThreads), count_args, 0, stream) !=
-      cudaSuccess)
-    return ZR_ERR_CUDA;
-  const int chunks = (int)((tiles + kChunkBins - 1) >> kChunkLog);
-  // With one chunk the scan needs no carry, so the chunk sums are skipped.
-  if (chunks > 1)
-    bin_chunk_sum_kernel<<<dim3((unsigned)chunks, (unsigned)n_parts), kScanThreads, 0, stream>>>(
-        cnt, (int)tiles, ctot);
-  bin_scan_kernel<<<dim3((unsigned)chunks, (unsigned)n_parts), kScanThreads, 0, stream>>>(
-      cnt, ctot, (int)tiles, excl, tot);
-  // per-warp counts and bases: 32 lanes (ballot) or one per partition
-  const size_t smem = (size_t)(kPartThreads / 32) * (ballot ? 32 : n_parts) * sizeof(long long);
-  const unsigned write_grid = (unsigned)grid_for(tiles, 8);
-  const void* write_fn = part_kernel<kIdentity>(false, nbits);
-  const long long* excl_c = excl;
-  const long long* tot_c = tot;
-  void* write_args[] = {(void*)&idx, (void*)&val, (void*)&nnz, (void*)&tiles, (void*)&h,
-                        (void*)&n_parts, (void*)&excl_c, (void*)&tot_c, (void*)&out_idx,
-                        (void*)&out_val, (void*)&d_offsets};
-  if (cudaLaunchKernel(write_fn, dim3(write_grid), dim3(kPartThreads), write_args, smem, stream) !=
-      cudaSuccess)
-    return ZR_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
-}
-}  // namespace
-
-zr_status partition_launch(const int32_t* idx, const float* val, int64_t nnz, int n_parts,
-                           uint64_t part_seed, int32_t* out_idx, float* out_val,
-                           int64_t* d_offsets, void* ws, cudaStream_t stream) {
-  return partition_run<false>(idx, val, nnz, n_parts, part_seed, out_idx, out_val, d_offsets, ws,
-                              stream);
-}
-
-zr_status index_sets_launch(int64_t m, int n_parts, uint64_t part_seed, int32_t* out_sets,
-                            int64_t* d_offsets, void* ws, cudaStream_t stream) {
-  return partition_run<true>(nullptr, nullptr, m, n_parts, part_seed, out_sets, nullptr, d_offsets,
-                             ws, stream);
 }
 
 }  // namespace zr

@@ -24,6 +24,12 @@
  *     launch errors (ZR_ERR_CUDA).  Errors found by a kernel on the device
  *     (an unsorted or out-of-range sparse index) are written to a status
  *     word inside `ws`; read it with zr_query_status after the stream work.
+ *   - zr_partition, zr_partition_static and zr_hash_index_sets are each one
+ *     cooperative launch whose CTAs wait for one another once.  That wait is bounded: if the CTAs cannot all run at
+ *     once (for example while another cooperative grid holds the device from
+ *     a stream that is not ordered with this one) it gives up after about a
+ *     second, the status word becomes ZR_ERR_TIMEOUT and the outputs are
+ *     unspecified.  Order such calls on one stream, or with events.
  *   - No C++ exception crosses this interface.
  */
 #ifndef ZR_H
@@ -237,7 +243,11 @@ zr_status zr_sparse_aggregate(const int32_t* const* idx, const float* const* val
                               int64_t* d_out_nnz, int64_t* d_offsets,
                               void* ws, size_t ws_bytes, void* stream);
 
-/* Workspace bytes zr_sparse_aggregate needs (0 on invalid arguments). */
+/* Workspace bytes zr_sparse_aggregate needs (0 on invalid arguments).  The
+ * kernels keep per-bin tables over the key range (bins of 1024 keys, wider
+ * for very large dense sizes): bin starts per rank and per-bin counts and
+ * positions per partition, so the size grows with dense_size * (n +
+ * n_parts), not with the entry count. */
 size_t zr_sparse_workspace_size(int32_t n, int64_t dense_size, int32_t n_parts);
 
 /*
@@ -257,7 +267,8 @@ zr_status zr_partition(const int32_t* idx, const float* val, int64_t nnz,
                        float* out_val, int64_t* d_offsets, void* ws,
                        size_t ws_bytes, void* stream);
 
-/* Workspace bytes zr_partition needs (0 on invalid arguments). */
+/* Workspace bytes zr_partition needs (0 on invalid arguments); like the
+ * union's, it does not grow with nnz (about 4 KB per partition). */
 size_t zr_partition_workspace_size(int64_t nnz, int32_t n_parts);
 
 /*
@@ -378,18 +389,31 @@ int32_t zr_choose_scheme(const int64_t* union_counts, int32_t n, double* gammas,
  *
  * Arguments and result are those of zr_partition minus ws / ws_bytes.  The
  * scratch is a fixed array of ZR_STATIC_SCRATCH_BYTES inside the library on
- * every device that loads it; a request whose
- * zr_partition_workspace_size(nnz, n_parts) exceeds that returns
- * ZR_ERR_CAPACITY and enqueues nothing.  The library never calls cudaMalloc
- * or cudaFree here.  The first call on a device (with that device current)
- * looks up the array's device address; make that first call before any
- * stream capture.  All calls on a device share the array (each call clears
- * what must start at zero), so calls that overlap on the GPU race.
+ * every device that loads it.  It holds what zr_partition_workspace_size
+ * asks for at every valid nnz and n_parts (at most about 1 MiB), so every
+ * valid request fits; a request that did not would return ZR_ERR_CAPACITY
+ * and enqueue nothing.  The library never calls cudaMalloc or cudaFree
+ * here.  The first call on a device (with that device current) looks up the
+ * array's device address and keeps it for the process; make that first call
+ * before any stream capture, and do not call this entry point on a device
+ * after cudaDeviceReset, which can move the array.  All calls on a device
+ * share the array (each call clears what must start at zero), so calls that
+ * overlap on the GPU race.
  */
 #define ZR_STATIC_SCRATCH_BYTES (2u << 20)
 zr_status zr_partition_static(const int32_t* idx, const float* val, int64_t nnz,
                               int32_t n_parts, uint64_t part_seed, int32_t* out_idx,
                               float* out_val, int64_t* d_offsets, void* stream);
+
+/*
+ * Testing only: makes the CTA with index `cta` skip its arrival at the grid
+ * wait of the next cooperative launches (zr_partition, zr_partition_static,
+ * zr_hash_index_sets), so that every other CTA's
+ * bounded wait runs out and the status word becomes ZR_ERR_TIMEOUT; -1 (the
+ * default) turns it off.  A process-wide setting, for tests of the timeout
+ * path; no GPU faults or hangs because of it.
+ */
+void zr_test_barrier_skip(int32_t cta);
 
 /*
  * Read the device status word at the start of a sparse workspace: waits for

@@ -67,8 +67,26 @@ def test_workspace_sizes(zr):
     a = zr.zr_sparse_workspace_size(8, 1 << 25, 8)
     b = zr.zr_sparse_workspace_size(8, 1 << 25, 16)
     assert 0 < a < b and a % 256 == 0
+    # the push-side partition's workspace: one count per (partition, CTA),
+    # independent of the entry count
     assert zr.zr_partition_workspace_size(1000, 0) == 0
     assert zr.zr_partition_workspace_size(1000, 8) > 0
+    assert zr.zr_partition_workspace_size(0, 8) == zr.zr_partition_workspace_size((1 << 31) - 1, 8)
+
+
+def test_static_scratch_holds_every_valid_partition_request(zr):
+    """The no-allocation entry's fixed scratch covers the workspace of every
+    valid request; the size is read from the header so the binding's copy
+    cannot drift from it."""
+    import re
+
+    hdr = open(os.path.join(ROOT, "include", "zr.h")).read()
+    m = re.search(r"#define ZR_STATIC_SCRATCH_BYTES \((\d+)u << (\d+)\)", hdr)
+    assert m, "ZR_STATIC_SCRATCH_BYTES not found in zr.h"
+    assert zr.ZR_STATIC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+    for parts in (1, 8, 16, 33, 255, zr.ZR_MAX_PARTS):
+        for nnz in (0, 1, 1 << 20, (1 << 31) - 1):
+            assert 0 < zr.zr_partition_workspace_size(nnz, parts) <= zr.ZR_STATIC_SCRATCH_BYTES
 
 
 def test_dense_argument_errors_before_launch(zr):
