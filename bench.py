@@ -1,21 +1,28 @@
 """Benchmark: aggregated gradient GB/s on one GB300 and its fraction of the
 HBM roofline, with the CPU oracle as the baseline.
 
-One step is one pass of the whole hot path over one batch of synthetic input:
-  1. dense ring all-reduce with the 1/N average, C2 workload: N = 8 ranks x
-     M = 25,557,032 fp32 (a ResNet-50-sized flat gradient), in place;
-  2. Random SkipReduce with skip fraction 0.5 (k = 4 of the 8 Reduce-Scatter
-     steps, seed 0, iteration count = the step number) on the same buffers;
-  3. sparse COO aggregation of the C4 embedding gradient (8 ranks x 335,544
-     entries over a dense size of 33,554,432, 60 % of entries in the first
-     1/8 of the range) into 8 h0 partitions;
-  4. the push-side h0 partition of rank 0's C4 list.
-Algorithmic ("roofline") bytes per step: dense (N-k)*M*4 read + N*M*4 written
-per call; sparse sum(nnz)*8 read + U*8 written + offsets; partition nnz*8 read
-and written.  GB/s = those bytes / device time; the roofline fraction divides
-by the measured HBM copy bandwidth.
+The timed step (the line's `value`) is the largest single-GPU
+configuration: Random SkipReduce on N = 8 ranks x M = 143,667,240 bf16 (a
+VGG-19-sized flat gradient, N(0, 1e-2) cast to bf16) at skip fractions 0,
+1/4 and 1/2, i.e. k = 0, 2 and 4 Reduce-Scatter steps skipped, one launch
+each, in place, seed 0, iteration count = the step number.  Algorithmic
+("roofline") bytes of a launch: (N - k) * M * 2 read + N * M * 2 written.
+GB/s = those bytes / device time; the roofline fraction divides by the
+measured HBM copy bandwidth.
+
+Every other configuration is timed in the same run, after the step, as a
+`part` with its bytes, median ms, GB/s and fraction: the N = 4, M = 2^20
+fp32 ring (C1), the ResNet-50-sized fp32 ring and SkipReduce (C2), the C4
+embedding-gradient union and push-side partition, the DGC top-5 % union
+(C5b), the dense fp32 sweep N x M (C5a) and the next-row kernels
+(AllReduce_Dropout, selective SkipReduce, Reduce-Scatter only, hash bitmap
+encode / decode / index sets, group densification).  A configuration whose
+inputs are smaller than twice the 129 MB L2 is timed over enough copies of
+its buffers (used in turn) that every launch reads HBM; the tiniest sweep
+points are latency-bound and flagged.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+       [--parts all|none|PREFIX[,PREFIX...]] [--no-e2e] [--no-cpu-baseline]
 With N > 1 (torchrun) every rank runs an independent replica of the whole
 workload on its own GPU (the path has no exchange between GPUs: replicas
 only); value = bytes of all ranks / the slowest rank's time.
@@ -38,30 +45,27 @@ if ROOT not in sys.path:
 METRIC = "aggregated gradient GB/s at 1 GB300 and % of HBM roofline, vs host-oracle"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-WORKLOAD = ("C2 dense ring all-reduce N=8 M=25,557,032 fp32 (plain + Random SkipReduce p=0.5) "
-            "+ C4 sparse COO union into 8 h0 partitions (N=8, M=33,554,432, 1% density) "
-            "+ push-side partition of one C4 list")
+L2_BYTES = 129 * 1000 * 1000
+WORKLOAD = ("C3 dense SkipReduce N=8 M=143,667,240 bf16 (VGG-19-sized), Random SkipReduce at "
+            "skip fractions 0, 1/4, 1/2 (k = 0, 2, 4), one in-place launch each per step")
 
 # DRAM traffic of the dominant kernel from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum per launch), valid only while the kernel source is the
-# one that was profiled.  The command that produced it is in profiles/.
+# one that was profiled (the ncu summary under profiles/ gives the command).
 TRAFFIC = {
-    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the full C2
-    # plain launch (profiles/ring_fused_kernel_c2_shape.md): 817.88 MB read
-    # + 760.58 MB written (the rest of the writes still sit in L2 at the end).
-    "ring_fused_kernel<float>": {"source_sha256": "65f1449d31f758edddd0132dab759b3887bf9c0889a74e467b28502acd62ad54",
-                                 "bytes_per_launch": 1_578_460_160},
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the C3 k = 0
+    # launch: 2,298,799,872 B read + 2,239,374,848 B written (the rest of the
+    # writes are still in L2 when the launch ends).
+    "ring_fused_kernel<bf16>": {
+        "source_sha256": "fb2c78050bb704767bc03b13c70c4983f16c37c746a451036e7291b8e04d9763",
+        "bytes_per_launch": 4_538_174_720},
 }
 
-# Kernel launches each library call makes (counted from the library source).
-# Kernels of this library launched per component per step (the status-word
-# memset of the sparse path is a runtime memset, not counted).
-LAUNCHES = {"ring": 1, "skip": 1, "rs_only": 1, "sparse": 5, "partition": 3, "dropout": 1,
-            "buckets": 1, "hb_encode": 3, "hb_decode": 3, "hb_sets": 4, "densify": 2}
-
-
-def torch_stream(torch):
-    return torch.cuda.current_stream().cuda_stream
+# Kernels of this library each call launches (counted from the library
+# source; the status-word memsets of the sparse paths are runtime memsets,
+# not counted).
+LAUNCHES = {"ring": 1, "skip": 1, "rs_only": 1, "dropout": 1, "buckets": 1, "union": 5,
+            "partition": 1, "hb_encode": 3, "hb_decode": 3, "hb_sets": 1, "densify": 2}
 
 
 def parse():
@@ -72,18 +76,9 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=("ring", "skip", "rs_only", "sparse", "partition", "dropout",
-                                       "buckets", "densify", "hb_encode", "hb_decode", "hb_sets"),
-                    default=None,
-                    help="profiling: time one component alone (prints a profiling line, not the "
-                         "benchmark line)")
-    ap.add_argument("--dense-m", type=int, default=None,
-                    help="profiling: elements per rank of the dense component (default C2's)")
-    ap.add_argument("--sparse", choices=("c4", "c5b"), default="c4",
-                    help="profiling: sparse workload for --only sparse/partition")
-    ap.add_argument("--profile", choices=("c3", "sweep"), default=None,
-                    help="profiling: the C3 bf16 SkipReduce launches (p = 0, 1/4, 1/2), or the "
-                         "dense fp32 sweep N x M; prints one profiling line")
+    ap.add_argument("--parts", default="all",
+                    help="the other configurations timed after the step: all, none, or "
+                         "comma-separated name prefixes (c1, c2, c4, c5a, c5b, next)")
     return ap.parse_args()
 
 
@@ -122,6 +117,16 @@ def max_over_ranks(ms, dist_mod, device):
 def job_throughput(step_bytes, steps, world, max_ms):
     """Whole-job GB/s: every replica processed step_bytes per step."""
     return world * step_bytes * steps / (max_ms / 1e3) / 1e9
+
+
+def rotation_sets(set_bytes, cap=2048):
+    """Copies of a configuration's buffers to use in turn so that their total
+    exceeds twice the L2 (every launch then reads HBM): one when a copy
+    alone does; capped, the capped case reported as L2-resident."""
+    if set_bytes >= 2 * L2_BYTES:
+        return 1, False
+    need = -(-2 * L2_BYTES // max(1, set_bytes)) + 1
+    return max(1, min(cap, need)), need > cap
 
 
 # ---------------------------------------------------------------- clocks
@@ -186,288 +191,95 @@ def summarize_clocks(lines):
             "samples": len(sm)}
 
 
-# ---------------------------------------------------------------- workload
-COMPONENTS = ("ring", "skip", "sparse", "partition")
+# ---------------------------------------------------------------- the step
+C3_KS = (0, 2, 4)
 
 
-class Workload:
-    """Device-resident inputs and outputs of one step (or of one component
-    when profiling with --only)."""
+class Step:
+    """The timed step's device buffers: the C3 bf16 rank buffers."""
 
-    def __init__(self, torch, zr, dev, only=None, dense_m=None, sparse="c4"):
+    def __init__(self, torch, zr, dev):
         import numpy as np
 
         import workloads
 
+        c = workloads.DENSE_C3
         self.torch, self.zr, self.dev = torch, zr, dev
-        self.components = (only,) if only else COMPONENTS
-        c2 = workloads.DENSE_C2
-        self.n, self.k = c2["n"], c2["skip_k"]
-        self.m = dense_m or c2["m"]
-        self.seed = c2["skip_seed"]
-        self.dense_on = any(c in self.components
-                            for c in ("ring", "skip", "rs_only", "dropout", "buckets"))
-        self.sparse_on = any(c in self.components
-                             for c in ("sparse", "partition", "hb_encode", "hb_decode", "hb_sets",
-                                       "densify"))
-        if self.dense_on:
-            if dense_m:
-                self.host_dense = workloads.dense_f32_per_rank(self.n, self.m, c2["sigma"], 200)
-            else:
-                self.host_dense = workloads.dense_c2()
-            self.dense = torch.from_numpy(self.host_dense).to(dev)
-            self.bufs = [self.dense[r] for r in range(self.n)]
-            # Selective SkipReduce: the flat gradient in 25 MB buckets (the
-            # DDP default size), the first bucket protected (k = 0), the
-            # others skipping k Reduce-Scatter steps (Random mode).
-            bucket = 25 * (1 << 20) // 4
-            self.buckets = []
-            for b, lo in enumerate(range(0, self.m, bucket)):
-                hi = min(lo + bucket, self.m)
-                self.buckets.append(dict(bufs=[self.dense[r, lo:hi] for r in range(self.n)],
-                                         k=0 if b == 0 else self.k, mode=zr.ZR_SKIP_RANDOM,
-                                         seed=self.seed + b, step=0, m=hi - lo))
-        if self.sparse_on:
-            cfg = workloads.SPARSE_C4 if sparse == "c4" else workloads.DGC_C5B
-            self.m4, self.parts = cfg["m"], cfg["n_parts"]
-            self.part_seed = cfg["part_seed"]
-            idx_l, val_l = workloads.sparse_c4() if sparse == "c4" else workloads.dgc_c5b()
-            self.sn = len(idx_l)
-            self.host_idx = [np.ascontiguousarray(a) for a in idx_l]
-            self.host_val = [np.ascontiguousarray(v) for v in val_l]
-            self.d_idx = [torch.from_numpy(a).to(dev) for a in self.host_idx]
-            self.d_val = [torch.from_numpy(v).to(dev) for v in self.host_val]
-            self.nnz = [int(a.size) for a in self.host_idx]
-            self.work = zr.SparseWorkspace(self.sn, self.m4, self.parts, sum(self.nnz), dev)
-            self.p_out_idx = torch.empty(self.nnz[0], dtype=torch.int32, device=dev)
-            self.p_out_val = torch.empty(self.nnz[0], dtype=torch.float32, device=dev)
-            self.p_off = torch.empty(self.parts + 1, dtype=torch.int64, device=dev)
-            self.p_ws = torch.empty(zr.zr_partition_workspace_size(self.nnz[0], self.parts),
-                                    dtype=torch.uint8, device=dev)
-            # The union size is fixed by the inputs: run once and read it.
-            zr.sparse_aggregate(self.d_idx, self.d_val, self.m4, self.parts, self.part_seed,
-                                work=self.work)
-            torch.cuda.synchronize()
-            self.union = int(self.work.out_nnz.item())
-            if "densify" in self.components:
-                # Zen's densification measurement: union sizes of every group
-                # of 2^L consecutive ranks, for the scheme choice
-                self.dn_ws = torch.empty(zr.zr_densification_workspace_size(self.sn, self.m4),
-                                         dtype=torch.uint8, device=dev)
-                self.dn_out = torch.empty(self.sn.bit_length(), dtype=torch.int64, device=dev)
-                self.dn_ptrs = [a.data_ptr() for a in self.d_idx]
-            if any(c in self.components for c in ("hb_encode", "hb_decode", "hb_sets")):
-                # Zen's Pull: every server's hash bitmap of the union's keys
-                self.hb = zr.HashBitmap(self.m4, self.parts, self.part_seed)
-                self.hb_keys = self.work.out_idx[:self.union]
-                self.hb.encode(self.hb_keys)
-                self.hb_out = torch.empty(self.union, dtype=torch.int32, device=dev)
-                self.hb_koff = torch.empty(self.parts + 1, dtype=torch.int64, device=dev)
-                self.hb_bits = self.hb.bits.clone()
-                self.hb_sets_ws = torch.empty(
-                    zr.zr_partition_workspace_size(self.m4, self.parts), dtype=torch.uint8,
-                    device=dev)
+        self.n, self.m = c["n"], c["m"]
+        self.host = workloads.dense_c3()  # uint16 bf16 bit patterns, (n, m)
+        h = torch.from_numpy(self.host.view(np.int16))
+        self.dense = h.to(dev).view(torch.bfloat16)
+        self.bufs = [self.dense[r] for r in range(self.n)]
+
+    def launch_bytes(self, k):
+        return (self.n - k) * self.m * 2 + self.n * self.m * 2
 
     def bytes(self):
-        s = 4
-        out = {}
-        if self.dense_on:
-            out["ring"] = 2 * self.n * self.m * s
-            out["skip"] = (self.n - self.k) * self.m * s + self.n * self.m * s
-            # Reduce-Scatter only: the folded ranks read, each slice written
-            # once, to its holder
-            out["rs_only"] = (self.n - self.k) * self.m * s + self.m * s
-            out["dropout"] = 2 * self.n * self.m * s
-            out["buckets"] = sum((self.n - b["k"]) * b["m"] * s + self.n * b["m"] * s
-                                 for b in self.buckets)
-        if self.sparse_on:
-            out["sparse"] = sum(self.nnz) * 8 + self.union * 8 + (self.parts + 1) * 8 + 8
-            out["partition"] = self.nnz[0] * 8 * 2 + (self.parts + 1) * 8
-            words = (self.m4 + 31) // 32
-            # encode: the index sets once, the keys once, the bitmaps out
-            out["hb_encode"] = self.m4 * 4 + self.union * 4 + words * 4
-            # decode: the bitmaps, the index-set entries of the set bits, the keys out
-            out["hb_decode"] = words * 4 + self.union * 4 * 2 + (self.parts + 1) * 8
-            # index sets: every index written once
-            out["hb_sets"] = self.m4 * 4 + (self.parts + 1) * 8
-            # densification: every key read once, the log2(n) + 1 counts out
-            out["densify"] = sum(self.nnz) * 4 + self.sn.bit_length() * 8
-        return {c: out[c] for c in self.components}
+        return sum(self.launch_bytes(k) for k in C3_KS)
 
-    def run(self, name, i):
+    def run(self, i, events=None, bufs=None):
         zr = self.zr
-        if name == "ring":
-            zr.ring_allreduce(self.bufs, average=True)
-        elif name == "skip":
-            zr.skipreduce(self.bufs, k=self.k, mode=zr.ZR_SKIP_RANDOM, seed=self.seed, step=i)
-        elif name == "rs_only":
-            zr.skipreduce(self.bufs, k=self.k, mode=zr.ZR_SKIP_RANDOM, seed=self.seed, step=i,
-                          rs_only=True)
-        elif name == "dropout":
-            zr.allreduce_dropout(self.bufs, 0.5, seed=self.seed, step=i)
-        elif name == "buckets":
-            zr.skipreduce_buckets([{k: v for k, v in dict(b, step=i).items() if k != "m"}
-                                   for b in self.buckets])
-        elif name == "hb_encode":
-            self.hb.encode(self.hb_keys)
-        elif name == "hb_decode":
-            self.hb.decode(self.hb_bits, self.hb_out, self.hb_koff)
-        elif name == "hb_sets":
-            zr.zr_hash_index_sets(self.m4, self.parts, self.part_seed, self.hb.sets.data_ptr(),
-                                  self.hb.offsets.data_ptr(), self.hb_sets_ws.data_ptr(),
-                                  self.hb_sets_ws.numel(), torch_stream(self.torch))
-        elif name == "densify":
-            zr.zr_densification(self.dn_ptrs, self.nnz, self.sn, self.m4, self.dn_out.data_ptr(),
-                                self.dn_ws.data_ptr(), self.dn_ws.numel(),
-                                torch_stream(self.torch))
-        elif name == "sparse":
-            zr.sparse_aggregate(self.d_idx, self.d_val, self.m4, self.parts, self.part_seed,
-                                work=self.work)
-        else:
-            zr.partition(self.d_idx[0], self.d_val[0], self.parts, self.part_seed,
-                         self.p_out_idx, self.p_out_val, self.p_off, self.p_ws)
-
-    def step(self, i, events=None):
-        """One pass; ``events`` maps component -> its end event (recorded on
-        the current stream, the one every call is launched on)."""
-        for name in self.components:
-            self.run(name, i)
+        for k in C3_KS:
+            zr.skipreduce(bufs or self.bufs, k=k, mode=zr.ZR_SKIP_RANDOM, seed=0, step=i)
             if events is not None:
-                events[name].record()
+                events[k].record()
 
 
-DENSE_PARTS = ("ring", "skip", "rs_only", "dropout", "buckets")
-
-
-def timed_overlap(torch, W, steps, warmup):
-    """The step with its dense components (HBM-bound ring kernels) on the
-    current stream and its sparse components (latency-bound) on a second
-    stream: they share no buffer, so they run side by side.  Every step
-    forks the second stream from the first and joins it back before the
-    next step begins, so steps never overlap each other."""
-    main = torch.cuda.current_stream()
-    side = torch.cuda.Stream()
-    dense = [c for c in W.components if c in DENSE_PARTS]
-    sparse = [c for c in W.components if c not in DENSE_PARTS]
-
-    def step(i):
-        fork = torch.cuda.Event()
-        fork.record(main)
-        side.wait_event(fork)
-        for name in dense:
-            W.run(name, i)
-        with torch.cuda.stream(side):
-            for name in sparse:
-                W.run(name, i)
-        join = torch.cuda.Event()
-        join.record(side)
-        main.wait_event(join)
-
+def timed_step(torch, S, steps, warmup):
+    """Device time of `steps` steps (CUDA events on the launching stream),
+    and each launch's own duration per k."""
     for i in range(warmup):
-        step(i)
+        S.run(i)
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(main)
-    for i in range(steps):
-        step(warmup + i)
-    end.record(main)
-    torch.cuda.synchronize()
-    return start.elapsed_time(end)
-
-
-def timed_device(torch, W, steps, warmup):
-    for i in range(warmup):
-        W.step(i)
-    torch.cuda.synchronize()
-    names = W.components
-    start = torch.cuda.Event(enable_timing=True)
-    evs = [{n: torch.cuda.Event(enable_timing=True) for n in names} for _ in range(steps)]
+    evs = [{k: torch.cuda.Event(enable_timing=True) for k in C3_KS} for _ in range(steps)]
     start.record()
     for i in range(steps):
-        W.step(warmup + i, evs[i])
+        S.run(warmup + i, evs[i])
     torch.cuda.synchronize()
-    total_ms = start.elapsed_time(evs[-1][names[-1]])
-    per = {n: [] for n in names}
+    total = start.elapsed_time(evs[-1][C3_KS[-1]])
+    per = {k: [] for k in C3_KS}
     prev = start
     for e in evs:
-        for n in names:
-            per[n].append(prev.elapsed_time(e[n]))  # each component starts where the last ended
-            prev = e[n]
-    return total_ms, per
+        for k in C3_KS:
+            per[k].append(prev.elapsed_time(e[k]))
+            prev = e[k]
+    return total, per
 
 
-def second_slot(torch, W):
-    """A copy of the step's device buffers (dense ranks, sparse inputs,
-    workspaces and outputs), so that two steps can be in flight."""
-    import copy
-
-    zr = W.zr
-    S = copy.copy(W)
-    if W.dense_on:
-        S.dense = torch.empty_like(W.dense)
-        S.bufs = [S.dense[r] for r in range(W.n)]
-    if W.sparse_on:
-        S.d_idx = [torch.empty_like(a) for a in W.d_idx]
-        S.d_val = [torch.empty_like(v) for v in W.d_val]
-        S.work = zr.SparseWorkspace(W.sn, W.m4, W.parts, sum(W.nnz), W.dev)
-        S.p_out_idx = torch.empty_like(W.p_out_idx)
-        S.p_out_val = torch.empty_like(W.p_out_val)
-        S.p_off = torch.empty_like(W.p_off)
-        S.p_ws = torch.empty_like(W.p_ws)
-    return S
-
-
-def timed_e2e(torch, W, steps):
+def timed_e2e(torch, S, steps):
     """The step through the public API from pinned host buffers: every step
-    copies its inputs host->device and reads its results back.  Steps are
-    pipelined over two buffer slots and three streams (copy in, compute,
-    copy out), so step i's copy-in overlaps step i - 1's compute and copy-out;
-    a slot is refilled only after its last copy-out has finished."""
+    copies the 8 rank buffers host->device, runs the three SkipReduce calls
+    and reads rank 0's result back.  Steps are pipelined over two device
+    buffer slots and three streams (copy in, compute, copy out); a slot is
+    refilled only after its last copy-out has finished."""
     import numpy as np
 
-    slots = [W, second_slot(torch, W)]
-    h_dense = torch.from_numpy(W.host_dense).pin_memory()
-    h_idx = [torch.from_numpy(a).pin_memory() for a in W.host_idx]
-    h_val = [torch.from_numpy(v).pin_memory() for v in W.host_val]
-    out_dense = torch.empty(W.m, dtype=torch.float32).pin_memory()
-    cap = sum(W.nnz)
-    out_idx = torch.empty(cap, dtype=torch.int32).pin_memory()
-    out_val = torch.empty(cap, dtype=torch.float32).pin_memory()
-    out_off = torch.empty(W.parts + 1, dtype=torch.int64).pin_memory()
-    p_idx = torch.empty(W.nnz[0], dtype=torch.int32).pin_memory()
-    p_val = torch.empty(W.nnz[0], dtype=torch.float32).pin_memory()
-    h2d = h_dense.numel() * 4 + sum(a.numel() * 8 for a in h_idx)
-    d2h = W.m * 4 + W.union * 8 + (W.parts + 1) * 8 + W.nnz[0] * 8
+    h_in = torch.from_numpy(S.host.view(np.int16)).pin_memory()
+    out = torch.empty(S.m, dtype=torch.int16).pin_memory()
+    slots = [S.dense, torch.empty_like(S.dense)]
+    h2d = h_in.numel() * 2
+    d2h = S.m * 2
     s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
     def run(first, count):
         done = {}
         for i in range(first, first + count):
-            S = slots[i % 2]
-            ev_in = torch.cuda.Event()
-            ev_comp = torch.cuda.Event()
-            ev_out = torch.cuda.Event()
+            d = slots[i % 2]
+            bufs = [d[r] for r in range(S.n)]
+            ev_in, ev_comp, ev_out = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
             with torch.cuda.stream(s_in):
                 if i - 2 in done:
                     s_in.wait_event(done[i - 2])
-                S.dense.copy_(h_dense, non_blocking=True)
-                for r in range(W.sn):
-                    S.d_idx[r].copy_(h_idx[r], non_blocking=True)
-                    S.d_val[r].copy_(h_val[r], non_blocking=True)
+                d.view(torch.int16).copy_(h_in, non_blocking=True)
                 ev_in.record(s_in)
             with torch.cuda.stream(s_comp):
                 s_comp.wait_event(ev_in)
-                S.step(i)
+                S.run(i, bufs=bufs)
                 ev_comp.record(s_comp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_comp)
-                out_dense.copy_(S.dense[0], non_blocking=True)
-                out_idx[:W.union].copy_(S.work.out_idx[:W.union], non_blocking=True)
-                out_val[:W.union].copy_(S.work.out_val[:W.union], non_blocking=True)
-                out_off.copy_(S.work.offsets[:W.parts + 1], non_blocking=True)
-                p_idx.copy_(S.p_out_idx, non_blocking=True)
-                p_val.copy_(S.p_out_val, non_blocking=True)
+                out.copy_(d[0].view(torch.int16), non_blocking=True)
                 ev_out.record(s_out)
             done[i] = ev_out
         return done
@@ -481,45 +293,289 @@ def timed_e2e(torch, W, steps):
     t1.record(s_out)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
-    assert np.isfinite(float(out_dense[0]))
+    got = torch.from_numpy(out.numpy().view(np.int16)).view(torch.bfloat16).float()
+    assert bool(torch.isfinite(got[:1000]).all())
+    del slots[1]
     return ms, h2d, d2h
+
+
+# ---------------------------------------------------------------- parts
+def time_calls(torch, calls, steps, warmup, graph=False):
+    """Median per-call device time (ms) of a list of calls used in turn (one
+    per copy of a configuration's buffers): each round runs every call once;
+    the round's time / len(calls) is one sample.  With graph=True the round
+    is captured in a CUDA graph and replayed (small launches are then timed
+    without the host's launch path)."""
+    for i in range(warmup):
+        for f in calls:
+            f(i)
+    torch.cuda.synchronize()
+    run = None
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for f in calls:
+                f(0)
+        run = g.replay
+        run()
+        torch.cuda.synchronize()
+    # back to back: an event after every round, no synchronisation between
+    # rounds, so the device queue stays full
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record()
+    for i in range(steps):
+        if run is not None:
+            run()
+        else:
+            for f in calls:
+                f(warmup + i)
+        evs[i + 1].record()
+    torch.cuda.synchronize()
+    times = [evs[i].elapsed_time(evs[i + 1]) / len(calls) for i in range(steps)]
+    return statistics.median(times)
+
+
+def part_entry(nbytes, ms, peak, **extra):
+    gbs = nbytes / (ms / 1e3) / 1e9
+    d = {"bytes": nbytes, "median_ms": ms, "gbs": gbs, "frac": gbs / peak}
+    d.update(extra)
+    return d
+
+
+def wanted(sel, name):
+    if sel == "all":
+        return True
+    if sel == "none":
+        return False
+    return any(name.startswith(p) for p in sel.split(","))
+
+
+def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
+    """Every configuration other than the step, one after another; returns
+    (parts, kernel launches made)."""
+    import numpy as np
+
+    import workloads
+
+    parts = {}
+    launches = 0
+
+    def free():
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+    # ---- C1: ring all-reduce, N = 4, M = 2^20 fp32, average (copies in turn)
+    if wanted(sel, "c1"):
+        c = workloads.DENSE_C1
+        n, m = c["n"], c["m"]
+        base = torch.from_numpy(workloads.dense_c1()).to(dev)
+        sets, resident = rotation_sets(n * m * 4)
+        copies = [base.clone() for _ in range(sets)]
+        calls = [(lambda i, x=x: zr.ring_allreduce([x[r] for r in range(n)], average=True))
+                 for x in copies]
+        ms = time_calls(torch, calls, steps, warmup, graph=True)
+        parts["c1_ring"] = part_entry(2 * n * m * 4, ms, peak, n=n, m=m, dtype="f32",
+                                      buffer_sets=sets, l2_resident=resident)
+        launches += (steps + warmup + 1) * sets
+        del base, copies, calls
+        free()
+
+    # ---- C2: ResNet-50-sized fp32 ring, SkipReduce and the next-row variants
+    if wanted(sel, "c2") or wanted(sel, "next"):
+        c = workloads.DENSE_C2
+        n, m, k = c["n"], c["m"], c["skip_k"]
+        x = torch.from_numpy(workloads.dense_c2()).to(dev)
+        bufs = [x[r] for r in range(n)]
+        items = []
+        if wanted(sel, "c2"):
+            items += [("c2_ring", lambda i: zr.ring_allreduce(bufs, average=True),
+                       2 * n * m * 4, "ring"),
+                      ("c2_skip_k4", lambda i: zr.skipreduce(bufs, k=k, mode=zr.ZR_SKIP_RANDOM,
+                                                             seed=c["skip_seed"], step=i),
+                       (2 * n - k) * m * 4, "skip")]
+        if wanted(sel, "next") or wanted(sel, "c2_next"):
+            bucket = 25 * (1 << 20) // 4
+            bks = []
+            for b, lo in enumerate(range(0, m, bucket)):
+                hi = min(lo + bucket, m)
+                bks.append(dict(bufs=[x[r, lo:hi] for r in range(n)], k=0 if b == 0 else k,
+                                mode=zr.ZR_SKIP_RANDOM, seed=b, step=0, m=hi - lo))
+            b_bytes = sum((n - b["k"]) * b["m"] * 4 + n * b["m"] * 4 for b in bks)
+            items += [
+                ("next_c2_rs_only_k4", lambda i: zr.skipreduce(bufs, k=k, mode=zr.ZR_SKIP_RANDOM,
+                                                               seed=0, step=i, rs_only=True),
+                 (n - k) * m * 4 + m * 4, "rs_only"),
+                ("next_c2_dropout_p50", lambda i: zr.allreduce_dropout(bufs, 0.5, seed=0, step=i),
+                 2 * n * m * 4, "dropout"),
+                ("next_c2_buckets", lambda i: zr.skipreduce_buckets(
+                    [{kk: v for kk, v in dict(bb, step=i).items() if kk != "m"} for bb in bks]),
+                 b_bytes, "buckets"),
+            ]
+        for name, fn, nbytes, kind in items:
+            ms = time_calls(torch, [fn], steps, warmup)
+            parts[name] = part_entry(nbytes, ms, peak, n=n, m=m, dtype="f32")
+            launches += (steps + warmup) * LAUNCHES[kind]
+        del x, bufs, items
+        free()
+
+    # ---- C4: embedding-gradient union and push-side partition, densification,
+    #      hash bitmaps (copies of the lists in turn where they fit in L2)
+    if wanted(sel, "c4") or wanted(sel, "next"):
+        c = workloads.SPARSE_C4
+        m, P, seed = c["m"], c["n_parts"], c["part_seed"]
+        idx_l, val_l = workloads.sparse_c4()
+        n = len(idx_l)
+        nnz = [a.size for a in idx_l]
+        in_bytes = sum(nnz) * 8
+        sets, resident = rotation_sets(in_bytes)
+        d_sets = []
+        for s in range(sets):
+            di = [torch.from_numpy(a).to(dev) for a in idx_l]
+            dv = [torch.from_numpy(v).to(dev) for v in val_l]
+            d_sets.append((di, dv, zr.SparseWorkspace(n, m, P, sum(nnz), dev)))
+        zr.sparse_aggregate(d_sets[0][0], d_sets[0][1], m, P, seed, work=d_sets[0][2])
+        torch.cuda.synchronize()
+        union = int(d_sets[0][2].out_nnz.item())
+        if wanted(sel, "c4"):
+            calls = [(lambda i, s=s: zr.sparse_aggregate(s[0], s[1], m, P, seed, work=s[2]))
+                     for s in d_sets]
+            ms = time_calls(torch, calls, steps, warmup, graph=True)
+            parts["c4_union"] = part_entry(in_bytes + union * 8 + (P + 1) * 8 + 8, ms, peak,
+                                           n=n, m=m, union=union, n_parts=P, buffer_sets=sets,
+                                           l2_resident=resident,
+                                           launches_per_call=LAUNCHES["union"])
+            launches += (steps + warmup + 1) * sets * LAUNCHES["union"]
+            p_out = [(torch.empty(nnz[0], dtype=torch.int32, device=dev),
+                      torch.empty(nnz[0], dtype=torch.float32, device=dev),
+                      torch.empty(P + 1, dtype=torch.int64, device=dev),
+                      torch.empty(zr.zr_partition_workspace_size(nnz[0], P), dtype=torch.uint8,
+                                  device=dev)) for _ in range(sets)]
+            calls = [(lambda i, s=s, o=o: zr.partition(s[0][0], s[1][0], P, seed, o[0], o[1], o[2],
+                                                        o[3])) for s, o in zip(d_sets, p_out)]
+            ms = time_calls(torch, calls, steps, warmup, graph=True)
+            parts["c4_partition"] = part_entry(nnz[0] * 16 + (P + 1) * 8, ms, peak, nnz=nnz[0],
+                                               n_parts=P, buffer_sets=sets, l2_resident=resident,
+                                               launches_per_call=LAUNCHES["partition"])
+            launches += (steps + warmup) * sets * LAUNCHES["partition"]
+            del p_out
+        if wanted(sel, "next") or wanted(sel, "c4_next"):
+            # group densification of the C4 lists (keys only)
+            dn = [(torch.empty(zr.zr_densification_workspace_size(n, m), dtype=torch.uint8,
+                               device=dev),
+                   torch.empty(n.bit_length(), dtype=torch.int64, device=dev)) for _ in d_sets]
+            stream = torch.cuda.current_stream().cuda_stream
+            calls = [(lambda i, s=s, w=w: zr.zr_densification(
+                [a.data_ptr() for a in s[0]], nnz, n, m, w[1].data_ptr(), w[0].data_ptr(),
+                w[0].numel(), stream)) for s, w in zip(d_sets, dn)]
+            ms = time_calls(torch, calls, steps, warmup)
+            parts["next_c4_densify"] = part_entry(sum(nnz) * 4 + n.bit_length() * 8, ms, peak,
+                                                  buffer_sets=sets, l2_resident=resident)
+            launches += (steps + warmup) * sets * LAUNCHES["densify"]
+            # Zen's Pull: hash bitmaps of the union's keys (index sets of 2^25 keys)
+            hb = zr.HashBitmap(m, P, seed)
+            keys = d_sets[0][2].out_idx[:union]
+            hb.encode(keys)
+            hb_out = torch.empty(union, dtype=torch.int32, device=dev)
+            hb_koff = torch.empty(P + 1, dtype=torch.int64, device=dev)
+            hb_bits = hb.bits.clone()
+            words = (m + 31) // 32
+            ms = time_calls(torch, [lambda i: hb.encode(keys)], steps, warmup)
+            parts["next_c4_hb_encode"] = part_entry(m * 4 + union * 4 + words * 4, ms, peak)
+            ms = time_calls(torch, [lambda i: hb.decode(hb_bits, hb_out, hb_koff)], steps, warmup)
+            parts["next_c4_hb_decode"] = part_entry(words * 4 + union * 8 + (P + 1) * 8, ms, peak)
+            sets_ws = torch.empty(zr.zr_partition_workspace_size(m, P), dtype=torch.uint8,
+                                  device=dev)
+            ms = time_calls(torch, [lambda i: zr.zr_hash_index_sets(
+                m, P, seed, hb.sets.data_ptr(), hb.offsets.data_ptr(), sets_ws.data_ptr(),
+                sets_ws.numel(), torch.cuda.current_stream().cuda_stream)], steps, warmup)
+            parts["next_c4_hb_sets"] = part_entry(m * 4 + (P + 1) * 8, ms, peak)
+            launches += (steps + warmup) * (LAUNCHES["hb_encode"] + LAUNCHES["hb_decode"]
+                                            + LAUNCHES["hb_sets"])
+            del hb, hb_out, hb_bits, dn
+        del d_sets
+        free()
+
+    # ---- C5b: DGC top-5 % lists of 16 ranks (288 MB of input: no copies needed)
+    if wanted(sel, "c5b") or wanted(sel, "next"):
+        c = workloads.DGC_C5B
+        m, P, seed = c["m"], c["n_parts"], c["part_seed"]
+        idx_l, val_l = workloads.dgc_c5b()
+        n = len(idx_l)
+        nnz = [a.size for a in idx_l]
+        di = [torch.from_numpy(a).to(dev) for a in idx_l]
+        dv = [torch.from_numpy(v).to(dev) for v in val_l]
+        work = zr.SparseWorkspace(n, m, P, sum(nnz), dev)
+        zr.sparse_aggregate(di, dv, m, P, seed, work=work)
+        torch.cuda.synchronize()
+        union = int(work.out_nnz.item())
+        if wanted(sel, "c5b"):
+            ms = time_calls(torch, [lambda i: zr.sparse_aggregate(di, dv, m, P, seed, work=work)],
+                            steps, warmup)
+            parts["c5b_union"] = part_entry(sum(nnz) * 8 + union * 8 + (P + 1) * 8 + 8, ms, peak,
+                                            n=n, m=m, union=union, n_parts=P,
+                                            launches_per_call=LAUNCHES["union"])
+            launches += (steps + warmup + 1) * LAUNCHES["union"]
+        if wanted(sel, "next") or wanted(sel, "c5b_next"):
+            w = torch.empty(zr.zr_densification_workspace_size(n, m), dtype=torch.uint8,
+                            device=dev)
+            o = torch.empty(n.bit_length(), dtype=torch.int64, device=dev)
+            stream = torch.cuda.current_stream().cuda_stream
+            ms = time_calls(torch, [lambda i: zr.zr_densification(
+                [a.data_ptr() for a in di], nnz, n, m, o.data_ptr(), w.data_ptr(), w.numel(),
+                stream)], steps, warmup)
+            parts["next_c5b_densify"] = part_entry(sum(nnz) * 4 + n.bit_length() * 8, ms, peak)
+            launches += (steps + warmup) * LAUNCHES["densify"]
+        del di, dv, work
+        free()
+
+    # ---- C5a: the dense fp32 sweep N x M, ring all-reduce with the 1/N average
+    if wanted(sel, "c5a"):
+        for n in workloads.SWEEP_NS:
+            for m in workloads.SWEEP_MS:
+                set_bytes = n * m * 4
+                sets, resident = rotation_sets(set_bytes)
+                x = workloads.dense_device(n, m * sets, 1e-3, 500 + n, dev)
+                # copy s is columns [s m, (s + 1) m) of every rank's row
+                calls = [(lambda i, s=s: zr.ring_allreduce(
+                    [x[r, s * m:(s + 1) * m] for r in range(n)], average=True))
+                    for s in range(sets)]
+                ms = time_calls(torch, calls, steps, warmup, graph=True)
+                parts["c5a_n%d_m2^%d" % (n, m.bit_length() - 1)] = part_entry(
+                    2 * n * m * 4, ms, peak, n=n, m=m, dtype="f32", buffer_sets=sets,
+                    l2_resident=resident)
+                launches += (steps + warmup + 1) * sets
+                del x, calls
+                free()
+    return parts, launches
 
 
 # ---------------------------------------------------------------- oracle
 def oracle_sample(budget_s=12.0):
     """Time the CPU oracle, as it stands, on a bounded sample of the step's
-    workload: the dense plain ring and the SkipReduce call on the first
-    M' elements of every C2 rank (M' a multiple of N), and the full C4 sparse
-    aggregation plus the partition of rank 0's list.  Returns a dict with
-    the GB/s over the sample's algorithmic bytes."""
-    import numpy as np
-
+    workload: the three Random SkipReduce calls (k = 0, 2, 4) of the C3
+    configuration on the first M' bf16 elements of every rank (M' a multiple
+    of N).  Returns a dict with the GB/s over the sample's algorithmic
+    bytes."""
     import workloads
     from oracle import ring as oring
-    from oracle import sparse as osparse
 
-    c2 = workloads.DENSE_C2
-    n, k = c2["n"], c2["skip_k"]
-    mp = (1 << 21)
-    x = workloads.dense_f32_per_rank(n, mp, c2["sigma"], 200)
-    c4 = workloads.SPARSE_C4
-    idx_l, val_l = workloads.sparse_c4()
+    c = workloads.DENSE_C3
+    n = c["n"]
+    mp = 1 << 20
+    x = workloads.dense_bf16_per_rank(n, mp, c["sigma"], 300)
     nbytes = 0
     t_total = 0.0
     reps = 0
     t_start = time.perf_counter()
     while True:
         t0 = time.perf_counter()
-        y = oring.allreduce_f32(x, divisor=oring.DIV_N)
-        o = oring.skip_offset(oring.SKIP_RANDOM, k, c2["skip_seed"], reps, n)
-        oring.allreduce_f32(y, k=k, o=o, divisor=oring.DIV_N)
-        ui, uv, off = osparse.aggregate(idx_l, val_l, c4["n_parts"], c4["part_seed"])
-        osparse.partition(idx_l[0], val_l[0], c4["n_parts"], c4["part_seed"])
+        y = x
+        for k in C3_KS:
+            o = oring.skip_offset(oring.SKIP_RANDOM, k, 0, reps, n)
+            y = oring.allreduce_bf16(y, k=k, o=o, divisor=oring.DIV_N)
+            nbytes += (n - k) * mp * 2 + n * mp * 2
         t_total += time.perf_counter() - t0
         reps += 1
-        nbytes += (2 * n * mp * 4 + (2 * n - k) * mp * 4 + sum(a.size for a in idx_l) * 8
-                   + ui.size * 8 + (c4["n_parts"] + 1) * 8 + 8 + idx_l[0].size * 16
-                   + (c4["n_parts"] + 1) * 8)
         if time.perf_counter() - t_start > budget_s:
             break
     return {
@@ -527,9 +583,9 @@ def oracle_sample(budget_s=12.0):
         "unit": UNIT,
         "cores": 1,
         "kind": "oracle",
-        "sample": ("%d repetitions of: literal ring + Random SkipReduce (k=4) on 8 ranks x %d fp32 "
-                   "(the first %d elements of each C2 rank), full C4 sparse union + 8-way partition "
-                   "and rank-0 push partition; numpy, single-threaded" % (reps, mp, mp)),
+        "sample": ("%d repetitions of the step's three Random SkipReduce calls (k = 0, 2, 4) on "
+                   "8 ranks x %d bf16 (the first %d elements of each C3 rank); literal ring, "
+                   "numpy, single-threaded" % (reps, mp, mp)),
         "seconds": t_total,
         "host_threads_available": len(os.sched_getaffinity(0)),
     }
@@ -542,7 +598,7 @@ def run_reference(args, rank, world):
     line = {
         "impl": "reference", "metric": METRIC, "value": res["value"], "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": {"workload": WORKLOAD, "sample": res["sample"]},
         "cpu_baseline": res,
         "e2e": {"value": res["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -554,89 +610,11 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------- main
-def time_launches(torch, fn, steps, warmup):
-    """Median CUDA-event time (ms) of ``fn`` over ``steps`` launches."""
-    for i in range(warmup):
-        fn(i)
-    torch.cuda.synchronize()
-    times = []
-    for i in range(steps):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn(warmup + i)
-        b.record()
-        b.synchronize()
-        times.append(a.elapsed_time(b))
-    return statistics.median(times)
-
-
-def run_profile(args):
-    """C3 and the C5a sweep: one profiling line each (not the benchmark line).
-    Inputs are drawn on the device with torch's seeded generator (the parity
-    tests draw them on the host from the workload definitions)."""
-    import torch
-
-    import __graft_entry__
-    import workloads
-
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    __graft_entry__.build()
-    import gradient_synchronisation_gb300 as zr
-
-    peak, _ = measured_hbm()
-    out = {"profiling": args.profile, "peak": peak, "steps": args.steps, "points": []}
-    if args.profile == "c3":
-        c = workloads.DENSE_C3
-        n, m = c["n"], c["m"]
-        g = torch.Generator(device=dev)
-        g.manual_seed(300)
-        x = (torch.randn((n, m), generator=g, device=dev) * c["sigma"]).to(torch.bfloat16)
-        bufs = [x[r] for r in range(n)]
-        for k in c["skip_ks"]:
-            ms = time_launches(torch, lambda i: zr.skipreduce(bufs, k=k, mode=zr.ZR_SKIP_RANDOM,
-                                                              seed=0, step=i),
-                               args.steps, args.warmup)
-            nbytes = (n - k) * m * 2 + n * m * 2
-            out["points"].append({"n": n, "m": m, "dtype": "bf16", "k": k, "bytes": nbytes,
-                                  "median_ms": ms, "gbs": nbytes / (ms / 1e3) / 1e9,
-                                  "frac": nbytes / (ms / 1e3) / 1e9 / peak})
-    else:
-        for n in workloads.SWEEP_NS:
-            for m in workloads.SWEEP_MS:
-                x = workloads.dense_device(n, m, 1e-3, 500 + n, dev)
-                bufs = [x[r] for r in range(n)]
-                # Captured in a CUDA graph and replayed, so that the time is
-                # the GPU's and not the host's launch path (which dominates at
-                # the small sizes).
-                reps = max(1, min(200, (1 << 26) // m))
-                zr.ring_allreduce(bufs, average=True)  # warm (and load) before capture
-                torch.cuda.synchronize()
-                graph = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(graph):
-                    for _ in range(reps):
-                        zr.ring_allreduce(bufs, average=True)
-                ms = time_launches(torch, lambda i: graph.replay(), args.steps, args.warmup) / reps
-                nbytes = 2 * n * m * 4
-                out["points"].append({"n": n, "m": m, "dtype": "f32", "bytes": nbytes,
-                                      "graph_reps": reps,
-                                      "median_ms": ms, "gbs": nbytes / (ms / 1e3) / 1e9,
-                                      "frac": nbytes / (ms / 1e3) / 1e9 / peak,
-                                      "l2_resident": nbytes < 129e6})
-                del x, bufs
-                torch.cuda.empty_cache()
-    print(json.dumps(out))
-    return 0
-
-
 def main():
     args = parse()
     rank, world, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
-    if args.profile:
-        return run_profile(args)
 
     import torch
 
@@ -652,67 +630,58 @@ def main():
     __graft_entry__.build()
     import gradient_synchronisation_gb300 as zr
 
-    W = Workload(torch, zr, dev, only=args.only, dense_m=args.dense_m, sparse=args.sparse)
-    b = W.bytes()
-    step_bytes = sum(b.values())
+    peak, peak_kind = measured_hbm()
+    S = Step(torch, zr, dev)
+    step_bytes = S.bytes()
 
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
-    # Sequential pass: every component alone on one stream (the per-component
-    # times and the ring kernel's roofline).  Then, for the full step, the
-    # timed pass that gives `value`: dense and sparse components on two
-    # streams, side by side inside each step.
-    seq_ms, per = timed_device(torch, W, args.steps, args.warmup)
-    overlap = not args.only and W.dense_on and W.sparse_on
-    total_ms = seq_ms
-    if overlap:
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        total_ms = timed_overlap(torch, W, args.steps, args.warmup)
-    clk = clocks.stop()
+    total_ms, per = timed_step(torch, S, args.steps, args.warmup)
     if world > 1:
         total_ms = max_over_ranks(total_ms, dist, dev)
-        seq_ms = max_over_ranks(seq_ms, dist, dev)
         dist.barrier()
     torch.cuda.synchronize()
+    step_clk = clocks.stop()
 
     value = job_throughput(step_bytes, args.steps, world, total_ms)
-    peak, peak_kind = measured_hbm()
     parts = {}
-    for name in W.components:
-        ms = statistics.median(per[name])
-        parts[name] = {"bytes": b[name], "median_ms": ms, "gbs": b[name] / (ms / 1e3) / 1e9,
-                       "frac": b[name] / (ms / 1e3) / 1e9 / peak}
-    if args.only:
-        if rank == 0:
-            print(json.dumps({"profiling": args.only, "dense_m": W.m if W.dense_on else None,
-                              "sparse": args.sparse if W.sparse_on else None,
-                              "steps": args.steps, "parts": parts, "peak": peak}))
-        return 0
+    for k in C3_KS:
+        ms = statistics.median(per[k])
+        parts["c3_k%d" % k] = part_entry(S.launch_bytes(k), ms, peak, n=S.n, m=S.m, dtype="bf16",
+                                         k=k, skip_fraction=k / S.n)
 
-    # Dominant kernel: ring_fused_kernel<float>.  achieved = the algorithmic
-    # bytes of its plain all-reduce launch (2*N*M*4) over that launch's mean
-    # CUDA-event duration; the SkipReduce launch of the same kernel is in
-    # parts["skip"].  The first timed launch follows the synchronize that
-    # opens the timed region, so its interval also holds the host's enqueue
-    # of the first step; the mean is over the launches after it.
-    ring_launches = per["ring"][1:] if len(per["ring"]) > 1 else per["ring"]
-    ring_ms = statistics.mean(ring_launches)
-    achieved = b["ring"] / (ring_ms / 1e3) / 1e9
-    tr = TRAFFIC["ring_fused_kernel<float>"]
+    # Dominant kernel: ring_fused_kernel<bf16>, the k = 0 launch (the plain
+    # ring with the average).  achieved = its algorithmic bytes over its
+    # mean CUDA-event duration; the first timed launch also holds the host's
+    # enqueue of the first step and is left out.
+    k0 = per[0][1:] if len(per[0]) > 1 else per[0]
+    ring_ms = statistics.mean(k0)
+    achieved = S.launch_bytes(0) / (ring_ms / 1e3) / 1e9
+    tr = TRAFFIC["ring_fused_kernel<bf16>"]
     sha = source_sha(os.path.join(ROOT, "gradient_synchronisation_gb300", "csrc", "ring.cu"))
     traffic = tr["bytes_per_launch"] if tr["source_sha256"] == sha else None
 
     e2e = None
     if not args.no_e2e:
-        e_ms, h2d, d2h = timed_e2e(torch, W, max(2, min(args.steps, 5)))
         steps_e = max(2, min(args.steps, 5))
+        e_ms, h2d, d2h = timed_e2e(torch, S, steps_e)
         e2e = {"value": world * step_bytes * steps_e / (e_ms / 1e3) / 1e9, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    del S
+    torch.cuda.empty_cache()
+    part_launches = 0
+    parts_clk = None
+    if args.parts != "none":
+        clocks = ClockSampler(torch.cuda.current_device())
+        clocks.start()
+        more, part_launches = run_parts(torch, zr, dev, args.parts, max(5, min(args.steps, 20)),
+                                        max(3, args.warmup), peak, None)
+        parts_clk = clocks.stop()
+        parts.update(more)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -722,26 +691,26 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
-            "ms_per_step_sequential": seq_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
             "config": {"workload": WORKLOAD, "bytes_per_step": step_bytes,
-                       "l2": "inputs larger than L2 (dense ranks 818 MB resident; the dense "
-                             "traffic evicts the sparse inputs between steps)",
+                       "l2": "inputs larger than L2 (8 rank buffers of 287 MB resident); the "
+                             "parts smaller than twice the L2 are timed over copies of their "
+                             "buffers used in turn (buffer_sets)",
                        "parallelism": "replicas only" if world > 1 else "single GPU",
-                       "streams": "dense components (ring, SkipReduce) and sparse components "
-                                  "(union, partition) on two streams, joined every step; "
-                                  "parts and roofline from a sequential pass of the same "
-                                  "steps"},
+                       "parts": "c3_* from the timed step; every other part timed after it, "
+                                "in the same process, median of CUDA-event samples"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "ring_fused_kernel<float>, C2 plain all-reduce launch",
-                         "launches_averaged": len(ring_launches),
-                         "peak_source": peak_kind},
+                         "kernel": "ring_fused_kernel<bf16>, C3 k = 0 launch",
+                         "launches_averaged": len(k0), "peak_source": peak_kind},
             "parts": parts,
             "e2e": e2e,
             "cpu_baseline": cpu,
-            "clocks": clk,
-            "gpu_launches": sum(LAUNCHES[c] for c in W.components) * args.steps,
+            "clocks": step_clk,
+            "clocks_parts": parts_clk,
+            "gpu_launches": len(C3_KS) * args.steps,
+            "gpu_launches_parts": part_launches,
         }
         print(json.dumps(line))
     if world > 1:

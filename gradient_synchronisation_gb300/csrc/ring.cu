@@ -79,6 +79,7 @@ constexpr int kSmallUnroll = 4;
 constexpr int kMediumFold = 6;
 constexpr int kMediumBatch = 6;
 constexpr int kMediumUnroll = 3;
+constexpr int64_t kOneWaveBytes = 64ll << 20;  // one-pass shape up to this launch size
 
 template <typename T>
 struct Elem;
@@ -323,10 +324,25 @@ zr_status launch_one(RingParams& P, cudaStream_t stream) {
                     : fold <= kSmallBatch  ? 1
                     : fold <= kMediumFold  ? 2
                                            : 3;
+  const bool drop = P.job.drop_thr != 0;
+  // Small launches (all rank buffers together at most kOneWaveBytes): one
+  // 16-byte vector per thread and a single pass, so every load of the
+  // launch is issued at once; the launch is latency-bound and this shape
+  // shortens it (C1, N = 4 x 2^20 fp32: 7.1 against 8.7 us).
+  constexpr int V = Elem<T>::kVec;
+  if (!drop && (int64_t)P.job.n * P.job.chunk * (int64_t)sizeof(T) <= kOneWaveBytes) {
+    const int64_t vpc = (P.job.chunk + V - 1) / V;
+    P.job.bps = (int)((vpc + kThreads - 1) / kThreads);
+    const dim3 g1((unsigned)P.job.bps, (unsigned)P.job.n);
+    if (fold <= kTinyFold) ring_fused_kernel<T, false, 1, kTinyBatch><<<g1, kThreads, 0, stream>>>(P);
+    else if (fold <= kSmallBatch) ring_fused_kernel<T, false, 1, kSmallBatch><<<g1, kThreads, 0, stream>>>(P);
+    else if (fold <= kMediumFold) ring_fused_kernel<T, false, 1, kMediumBatch><<<g1, kThreads, 0, stream>>>(P);
+    else ring_fused_kernel<T, false, 1, kBatch><<<g1, kThreads, 0, stream>>>(P);
+    return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
+  }
   const int unroll[4] = {kTinyUnroll, kSmallUnroll, kMediumUnroll, kUnroll};
   P.job.bps = blocks_per_slice<T>(P.job.chunk, unroll[shape]);
   dim3 grid((unsigned)P.job.bps, (unsigned)P.job.n);
-  const bool drop = P.job.drop_thr != 0;
   switch (shape * 2 + (drop ? 1 : 0)) {
     case 0: ring_fused_kernel<T, false, kTinyUnroll, kTinyBatch><<<grid, kThreads, 0, stream>>>(P); break;
     case 1: ring_fused_kernel<T, true, kTinyUnroll, kTinyBatch><<<grid, kThreads, 0, stream>>>(P); break;
