@@ -51,7 +51,7 @@ WORKLOAD = ("C3 dense SkipReduce N=8 M=143,667,240 bf16 (VGG-19-sized), Random S
 
 # DRAM traffic of the dominant kernel from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum per launch), valid only while the kernel source is the
-# one that was profiled (the ncu summary under profiles/ gives the command).
+# one that was profiled.
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the C3 k = 0
     # launch: 2,298,799,872 B read + 2,239,374,848 B written (the rest of the
@@ -79,6 +79,9 @@ def parse():
     ap.add_argument("--parts", default="all",
                     help="the other configurations timed after the step: all, none, or "
                          "comma-separated name prefixes (c1, c2, c4, c5a, c5b, next)")
+    ap.add_argument("--parts-only", action="store_true",
+                    help="profiling: time only the selected parts (no step, no benchmark "
+                         "line; prints one profiling line)")
     return ap.parse_args()
 
 
@@ -343,11 +346,13 @@ def part_entry(nbytes, ms, peak, **extra):
 
 
 def wanted(sel, name):
+    """Part `name` is selected (a prefix of it is), or, for a group prefix
+    such as "c4", some part under it is."""
     if sel == "all":
         return True
     if sel == "none":
         return False
-    return any(name.startswith(p) for p in sel.split(","))
+    return any(name.startswith(p) or p.startswith(name) for p in sel.split(","))
 
 
 def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
@@ -365,7 +370,7 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
         torch.cuda.empty_cache()
 
     # ---- C1: ring all-reduce, N = 4, M = 2^20 fp32, average (copies in turn)
-    if wanted(sel, "c1"):
+    if wanted(sel, "c1_ring"):
         c = workloads.DENSE_C1
         n, m = c["n"], c["m"]
         base = torch.from_numpy(workloads.dense_c1()).to(dev)
@@ -381,19 +386,17 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
         free()
 
     # ---- C2: ResNet-50-sized fp32 ring, SkipReduce and the next-row variants
-    if wanted(sel, "c2") or wanted(sel, "next"):
+    if wanted(sel, "c2_") or wanted(sel, "next_c2"):
         c = workloads.DENSE_C2
         n, m, k = c["n"], c["m"], c["skip_k"]
         x = torch.from_numpy(workloads.dense_c2()).to(dev)
         bufs = [x[r] for r in range(n)]
-        items = []
-        if wanted(sel, "c2"):
-            items += [("c2_ring", lambda i: zr.ring_allreduce(bufs, average=True),
-                       2 * n * m * 4, "ring"),
-                      ("c2_skip_k4", lambda i: zr.skipreduce(bufs, k=k, mode=zr.ZR_SKIP_RANDOM,
-                                                             seed=c["skip_seed"], step=i),
-                       (2 * n - k) * m * 4, "skip")]
-        if wanted(sel, "next") or wanted(sel, "c2_next"):
+        items = [("c2_ring", lambda i: zr.ring_allreduce(bufs, average=True),
+                  2 * n * m * 4, "ring"),
+                 ("c2_skip_k4", lambda i: zr.skipreduce(bufs, k=k, mode=zr.ZR_SKIP_RANDOM,
+                                                        seed=c["skip_seed"], step=i),
+                  (2 * n - k) * m * 4, "skip")]
+        if wanted(sel, "next_c2"):
             bucket = 25 * (1 << 20) // 4
             bks = []
             for b, lo in enumerate(range(0, m, bucket)):
@@ -412,6 +415,8 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
                  b_bytes, "buckets"),
             ]
         for name, fn, nbytes, kind in items:
+            if not wanted(sel, name):
+                continue
             ms = time_calls(torch, [fn], steps, warmup)
             parts[name] = part_entry(nbytes, ms, peak, n=n, m=m, dtype="f32")
             launches += (steps + warmup) * LAUNCHES[kind]
@@ -420,7 +425,7 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
 
     # ---- C4: embedding-gradient union and push-side partition, densification,
     #      hash bitmaps (copies of the lists in turn where they fit in L2)
-    if wanted(sel, "c4") or wanted(sel, "next"):
+    if wanted(sel, "c4_") or wanted(sel, "next_c4"):
         c = workloads.SPARSE_C4
         m, P, seed = c["m"], c["n_parts"], c["part_seed"]
         idx_l, val_l = workloads.sparse_c4()
@@ -436,7 +441,7 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
         zr.sparse_aggregate(d_sets[0][0], d_sets[0][1], m, P, seed, work=d_sets[0][2])
         torch.cuda.synchronize()
         union = int(d_sets[0][2].out_nnz.item())
-        if wanted(sel, "c4"):
+        if wanted(sel, "c4_union"):
             calls = [(lambda i, s=s: zr.sparse_aggregate(s[0], s[1], m, P, seed, work=s[2]))
                      for s in d_sets]
             ms = time_calls(torch, calls, steps, warmup, graph=True)
@@ -445,6 +450,7 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
                                            l2_resident=resident,
                                            launches_per_call=LAUNCHES["union"])
             launches += (steps + warmup + 1) * sets * LAUNCHES["union"]
+        if wanted(sel, "c4_partition"):
             p_out = [(torch.empty(nnz[0], dtype=torch.int32, device=dev),
                       torch.empty(nnz[0], dtype=torch.float32, device=dev),
                       torch.empty(P + 1, dtype=torch.int64, device=dev),
@@ -458,7 +464,7 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
                                                launches_per_call=LAUNCHES["partition"])
             launches += (steps + warmup) * sets * LAUNCHES["partition"]
             del p_out
-        if wanted(sel, "next") or wanted(sel, "c4_next"):
+        if wanted(sel, "next_c4_densify"):
             # group densification of the C4 lists (keys only)
             dn = [(torch.empty(zr.zr_densification_workspace_size(n, m), dtype=torch.uint8,
                                device=dev),
@@ -471,6 +477,8 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
             parts["next_c4_densify"] = part_entry(sum(nnz) * 4 + n.bit_length() * 8, ms, peak,
                                                   buffer_sets=sets, l2_resident=resident)
             launches += (steps + warmup) * sets * LAUNCHES["densify"]
+            del dn
+        if wanted(sel, "next_c4_hb"):
             # Zen's Pull: hash bitmaps of the union's keys (index sets of 2^25 keys)
             hb = zr.HashBitmap(m, P, seed)
             keys = d_sets[0][2].out_idx[:union]
@@ -491,12 +499,12 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
             parts["next_c4_hb_sets"] = part_entry(m * 4 + (P + 1) * 8, ms, peak)
             launches += (steps + warmup) * (LAUNCHES["hb_encode"] + LAUNCHES["hb_decode"]
                                             + LAUNCHES["hb_sets"])
-            del hb, hb_out, hb_bits, dn
+            del hb, hb_out, hb_bits
         del d_sets
         free()
 
     # ---- C5b: DGC top-5 % lists of 16 ranks (288 MB of input: no copies needed)
-    if wanted(sel, "c5b") or wanted(sel, "next"):
+    if wanted(sel, "c5b") or wanted(sel, "next_c5b"):
         c = workloads.DGC_C5B
         m, P, seed = c["m"], c["n_parts"], c["part_seed"]
         idx_l, val_l = workloads.dgc_c5b()
@@ -508,14 +516,14 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
         zr.sparse_aggregate(di, dv, m, P, seed, work=work)
         torch.cuda.synchronize()
         union = int(work.out_nnz.item())
-        if wanted(sel, "c5b"):
+        if wanted(sel, "c5b_union"):
             ms = time_calls(torch, [lambda i: zr.sparse_aggregate(di, dv, m, P, seed, work=work)],
                             steps, warmup)
             parts["c5b_union"] = part_entry(sum(nnz) * 8 + union * 8 + (P + 1) * 8 + 8, ms, peak,
                                             n=n, m=m, union=union, n_parts=P,
                                             launches_per_call=LAUNCHES["union"])
             launches += (steps + warmup + 1) * LAUNCHES["union"]
-        if wanted(sel, "next") or wanted(sel, "c5b_next"):
+        if wanted(sel, "next_c5b_densify"):
             w = torch.empty(zr.zr_densification_workspace_size(n, m), dtype=torch.uint8,
                             device=dev)
             o = torch.empty(n.bit_length(), dtype=torch.int64, device=dev)
@@ -532,6 +540,9 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
     if wanted(sel, "c5a"):
         for n in workloads.SWEEP_NS:
             for m in workloads.SWEEP_MS:
+                name = "c5a_n%d_m2^%d" % (n, m.bit_length() - 1)
+                if not wanted(sel, name):
+                    continue
                 set_bytes = n * m * 4
                 sets, resident = rotation_sets(set_bytes)
                 x = workloads.dense_device(n, m * sets, 1e-3, 500 + n, dev)
@@ -540,7 +551,7 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
                     [x[r, s * m:(s + 1) * m] for r in range(n)], average=True))
                     for s in range(sets)]
                 ms = time_calls(torch, calls, steps, warmup, graph=True)
-                parts["c5a_n%d_m2^%d" % (n, m.bit_length() - 1)] = part_entry(
+                parts[name] = part_entry(
                     2 * n * m * 4, ms, peak, n=n, m=m, dtype="f32", buffer_sets=sets,
                     l2_resident=resident)
                 launches += (steps + warmup + 1) * sets
@@ -631,6 +642,13 @@ def main():
     import gradient_synchronisation_gb300 as zr
 
     peak, peak_kind = measured_hbm()
+    if args.parts_only:
+        parts, n_launch = run_parts(torch, zr, dev, args.parts, max(1, args.steps),
+                                    max(1, args.warmup), peak, None)
+        if rank == 0:
+            print(json.dumps({"profiling": args.parts, "steps": args.steps, "peak": peak,
+                              "parts": parts, "gpu_launches": n_launch}))
+        return 0
     S = Step(torch, zr, dev)
     step_bytes = S.bytes()
 
