@@ -65,7 +65,8 @@ TRAFFIC = {
 # source; the status-word memsets of the sparse paths are runtime memsets,
 # not counted).
 LAUNCHES = {"ring": 1, "skip": 1, "rs_only": 1, "dropout": 1, "buckets": 1, "union": 5,
-            "partition": 1, "hb_encode": 3, "hb_decode": 3, "hb_sets": 1, "densify": 2}
+            "partition": 1, "hb_directory": 2, "hb_encode": 2, "hb_decode": 3, "hb_sets": 1,
+            "densify": 2}
 
 
 def parse():
@@ -479,7 +480,10 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
             launches += (steps + warmup) * sets * LAUNCHES["densify"]
             del dn
         if wanted(sel, "next_c4_hb"):
-            # Zen's Pull: hash bitmaps of the union's keys (index sets of 2^25 keys)
+            # Zen's Pull: hash bitmaps of the union's keys over M = 2^25.  The
+            # encode / decode recompute h0 for all M indices (bound by that
+            # arithmetic: hashes_per_s); their bytes are the keys and the
+            # bitmaps.
             hb = zr.HashBitmap(m, P, seed)
             keys = d_sets[0][2].out_idx[:union]
             hb.encode(keys)
@@ -487,19 +491,29 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
             hb_koff = torch.empty(P + 1, dtype=torch.int64, device=dev)
             hb_bits = hb.bits.clone()
             words = (m + 31) // 32
+            dir_bytes = zr.zr_hash_directory_size(m, P)
+            stream = torch.cuda.current_stream().cuda_stream
+            ms = time_calls(torch, [lambda i: zr.zr_hash_directory(
+                m, P, seed, hb.directory.data_ptr(), dir_bytes, stream)], steps, warmup)
+            parts["next_c4_hb_directory"] = part_entry(dir_bytes, ms, peak,
+                                                       hashes_per_s=m / (ms / 1e3))
             ms = time_calls(torch, [lambda i: hb.encode(keys)], steps, warmup)
-            parts["next_c4_hb_encode"] = part_entry(m * 4 + union * 4 + words * 4, ms, peak)
+            parts["next_c4_hb_encode"] = part_entry(union * 4 + words * 4 + (P + 1) * 8, ms, peak,
+                                                    hashes_per_s=m / (ms / 1e3))
             ms = time_calls(torch, [lambda i: hb.decode(hb_bits, hb_out, hb_koff)], steps, warmup)
-            parts["next_c4_hb_decode"] = part_entry(words * 4 + union * 8 + (P + 1) * 8, ms, peak)
+            parts["next_c4_hb_decode"] = part_entry(words * 4 + union * 4 + (P + 1) * 8, ms, peak,
+                                                    hashes_per_s=m / (ms / 1e3))
+            sets = torch.empty(m, dtype=torch.int32, device=dev)
+            offs = torch.empty(P + 1, dtype=torch.int64, device=dev)
             sets_ws = torch.empty(zr.zr_partition_workspace_size(m, P), dtype=torch.uint8,
                                   device=dev)
             ms = time_calls(torch, [lambda i: zr.zr_hash_index_sets(
-                m, P, seed, hb.sets.data_ptr(), hb.offsets.data_ptr(), sets_ws.data_ptr(),
-                sets_ws.numel(), torch.cuda.current_stream().cuda_stream)], steps, warmup)
+                m, P, seed, sets.data_ptr(), offs.data_ptr(), sets_ws.data_ptr(),
+                sets_ws.numel(), stream)], steps, warmup)
             parts["next_c4_hb_sets"] = part_entry(m * 4 + (P + 1) * 8, ms, peak)
-            launches += (steps + warmup) * (LAUNCHES["hb_encode"] + LAUNCHES["hb_decode"]
-                                            + LAUNCHES["hb_sets"])
-            del hb, hb_out, hb_bits
+            launches += (steps + warmup) * (LAUNCHES["hb_directory"] + LAUNCHES["hb_encode"]
+                                            + LAUNCHES["hb_decode"] + LAUNCHES["hb_sets"])
+            del hb, hb_out, hb_bits, sets, sets_ws
         del d_sets
         free()
 

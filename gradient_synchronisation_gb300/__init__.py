@@ -47,6 +47,7 @@ ZR_DIV_N_MINUS_K = 1
 ZR_DIV_NONE = 2
 ZR_MAX_RANKS = 64
 ZR_MAX_PARTS = 256
+ZR_HASH_RANGE = 2048
 ZR_SKIP_RS_ONLY = 1
 ZR_MAX_BUCKETS = 128
 ZR_MAX_BUCKET_BUFS = 2048
@@ -55,7 +56,8 @@ EXPORTS = (
     "zr_ring_allreduce", "zr_skipreduce", "zr_sparse_aggregate", "zr_sparse_workspace_size",
     "zr_partition", "zr_partition_workspace_size", "zr_query_status", "zr_status_string",
     "zr_version", "zr_partition_static", "zr_skipreduce_buckets", "zr_allreduce_dropout",
-    "zr_hash_index_sets", "zr_hash_bitmap_encode", "zr_hash_bitmap_decode",
+    "zr_hash_index_sets", "zr_hash_directory", "zr_hash_directory_size",
+    "zr_hash_bitmap_encode", "zr_hash_bitmap_decode",
     "zr_hash_bitmap_workspace_size", "zr_densification", "zr_densification_workspace_size",
     "zr_choose_scheme", "zr_test_barrier_skip",
 )
@@ -104,8 +106,10 @@ def _load():
         "zr_skipreduce_buckets": (i32, [ctypes.POINTER(Bucket), i32, i32, i32, P]),
         "zr_allreduce_dropout": (i32, [PP, i32, i64, i32, u64, u64, u64, i32, P]),
         "zr_hash_index_sets": (i32, [i64, i32, u64, P, P, P, sz, P]),
-        "zr_hash_bitmap_encode": (i32, [P, P, i64, i32, P, i64, P, i64, P, P, sz, P]),
-        "zr_hash_bitmap_decode": (i32, [P, P, i64, i32, P, P, i64, P, P, sz, P]),
+        "zr_hash_directory": (i32, [i64, i32, u64, P, sz, P]),
+        "zr_hash_directory_size": (sz, [i64, i32]),
+        "zr_hash_bitmap_encode": (i32, [P, i64, i32, u64, P, i64, P, i64, P, P, sz, P]),
+        "zr_hash_bitmap_decode": (i32, [P, i64, i32, u64, P, P, i64, P, P, sz, P]),
         "zr_hash_bitmap_workspace_size": (sz, [i64, i32]),
         "zr_densification": (i32, [PP, ctypes.POINTER(i64), i32, i64, P, P, sz, P]),
         "zr_densification_workspace_size": (sz, [i32, i64]),
@@ -171,20 +175,28 @@ def zr_hash_index_sets(dense_size, n_parts, part_seed, out_sets, d_offsets, ws, 
                                     ws_bytes, stream)
 
 
+def zr_hash_directory_size(dense_size, n_parts):
+    return lib().zr_hash_directory_size(dense_size, n_parts)
+
+
+def zr_hash_directory(dense_size, n_parts, part_seed, d_dir, dir_bytes, stream):
+    return lib().zr_hash_directory(dense_size, n_parts, part_seed, d_dir, dir_bytes, stream)
+
+
 def zr_hash_bitmap_workspace_size(dense_size, n_parts):
     return lib().zr_hash_bitmap_workspace_size(dense_size, n_parts)
 
 
-def zr_hash_bitmap_encode(sets, d_set_offsets, dense_size, n_parts, keys, n_keys, out_bits,
+def zr_hash_bitmap_encode(d_dir, dense_size, n_parts, part_seed, keys, n_keys, out_bits,
                           out_cap_words, d_word_offsets, ws, ws_bytes, stream):
-    return lib().zr_hash_bitmap_encode(sets, d_set_offsets, dense_size, n_parts, keys, n_keys,
+    return lib().zr_hash_bitmap_encode(d_dir, dense_size, n_parts, part_seed, keys, n_keys,
                                        out_bits, out_cap_words, d_word_offsets, ws, ws_bytes,
                                        stream)
 
 
-def zr_hash_bitmap_decode(sets, d_set_offsets, dense_size, n_parts, bits, out_keys, out_cap,
+def zr_hash_bitmap_decode(d_dir, dense_size, n_parts, part_seed, bits, out_keys, out_cap,
                           d_key_offsets, ws, ws_bytes, stream):
-    return lib().zr_hash_bitmap_decode(sets, d_set_offsets, dense_size, n_parts, bits, out_keys,
+    return lib().zr_hash_bitmap_decode(d_dir, dense_size, n_parts, part_seed, bits, out_keys,
                                        out_cap, d_key_offsets, ws, ws_bytes, stream)
 
 
@@ -419,35 +431,32 @@ def partition(idx, val, n_parts, part_seed=0, out_idx=None, out_val=None, offset
 
 # ------------------------------------------------------------ hash bitmap
 class HashBitmap:
-    """Zen's index sets I_p of a dense size and partition count, built once on
-    the device, and the encode / decode calls that use them.  ``bits`` and
-    ``keys`` results are torch tensors (bitmap words stored as int32)."""
+    """Zen's hash bitmaps of a dense size, partition count and h0 seed: the
+    directory of index-set counts built once on the device, and the encode /
+    decode calls that use it.  ``bits`` and ``keys`` results are torch
+    tensors (bitmap words stored as int32)."""
 
     def __init__(self, dense_size, n_parts, part_seed=0, device="cuda", stream=None):
         import torch
 
         self.m, self.parts, self.seed = dense_size, n_parts, part_seed
-        self.sets = torch.empty(dense_size, dtype=torch.int32, device=device)
-        self.offsets = torch.empty(n_parts + 1, dtype=torch.int64, device=device)
-        ws = torch.empty(max(16, zr_partition_workspace_size(dense_size, n_parts)),
-                         dtype=torch.uint8, device=device)
-        _check(zr_hash_index_sets(dense_size, n_parts, part_seed, self.sets.data_ptr(),
-                                  self.offsets.data_ptr(), ws.data_ptr(), ws.numel(),
-                                  _stream(stream)), "zr_hash_index_sets")
+        n_dir = zr_hash_directory_size(dense_size, n_parts)
         n_ws = zr_hash_bitmap_workspace_size(dense_size, n_parts)
-        if n_ws == 0:
+        if n_dir == 0 or n_ws == 0:
             raise ValueError("invalid hash bitmap request")
+        self.directory = torch.empty(n_dir // 4, dtype=torch.int32, device=device)
+        _check(zr_hash_directory(dense_size, n_parts, part_seed, self.directory.data_ptr(), n_dir,
+                                 _stream(stream)), "zr_hash_directory")
         self.ws = torch.empty(n_ws, dtype=torch.uint8, device=device)
         self.cap_words = (dense_size + 31) // 32 + n_parts
         self.bits = torch.empty(self.cap_words, dtype=torch.int32, device=device)
         self.word_offsets = torch.empty(n_parts + 1, dtype=torch.int64, device=device)
-        self._keep = ws
 
     def encode(self, keys, stream=None):
         """Bitmaps of the nonzero indices ``keys`` (int32 CUDA tensor)."""
-        _check(zr_hash_bitmap_encode(self.sets.data_ptr(), self.offsets.data_ptr(), self.m,
-                                     self.parts, keys.data_ptr() if keys.numel() else None,
-                                     keys.numel(), self.bits.data_ptr(), self.cap_words,
+        _check(zr_hash_bitmap_encode(self.directory.data_ptr(), self.m, self.parts, self.seed,
+                                     keys.data_ptr() if keys.numel() else None, keys.numel(),
+                                     self.bits.data_ptr(), self.cap_words,
                                      self.word_offsets.data_ptr(), self.ws.data_ptr(),
                                      self.ws.numel(), _stream(stream)), "zr_hash_bitmap_encode")
         return self.bits, self.word_offsets
@@ -456,14 +465,29 @@ class HashBitmap:
         """Indices of the set bits of ``bits`` (laid out as ``encode``
         writes them) into ``out_keys``; partition offsets into
         ``key_offsets``."""
-        _check(zr_hash_bitmap_decode(self.sets.data_ptr(), self.offsets.data_ptr(), self.m,
-                                     self.parts, bits.data_ptr(), out_keys.data_ptr(),
-                                     out_keys.numel(), key_offsets.data_ptr(), self.ws.data_ptr(),
-                                     self.ws.numel(), _stream(stream)), "zr_hash_bitmap_decode")
+        _check(zr_hash_bitmap_decode(self.directory.data_ptr(), self.m, self.parts, self.seed,
+                                     bits.data_ptr(), out_keys.data_ptr(), out_keys.numel(),
+                                     key_offsets.data_ptr(), self.ws.data_ptr(), self.ws.numel(),
+                                     _stream(stream)), "zr_hash_bitmap_decode")
         return out_keys, key_offsets
 
     def status(self, stream=None):
         return zr_query_status(self.ws.data_ptr(), _stream(stream))
+
+
+def hash_index_sets(dense_size, n_parts, part_seed=0, device="cuda", stream=None):
+    """Zen's index sets I_p of [0, dense_size) on the device: (sets, offsets)
+    with I_p = sets[offsets[p]:offsets[p+1]], each ascending."""
+    import torch
+
+    sets = torch.empty(dense_size, dtype=torch.int32, device=device)
+    offsets = torch.empty(n_parts + 1, dtype=torch.int64, device=device)
+    ws = torch.empty(max(16, zr_partition_workspace_size(dense_size, n_parts)),
+                     dtype=torch.uint8, device=device)
+    _check(zr_hash_index_sets(dense_size, n_parts, part_seed, sets.data_ptr(), offsets.data_ptr(),
+                              ws.data_ptr(), ws.numel(), _stream(stream)), "zr_hash_index_sets")
+    torch.cuda.synchronize()  # one-time build; the workspace is freed on return
+    return sets, offsets
 
 
 def densification(idx_list, dense_size, stream=None):

@@ -148,39 +148,53 @@ zr_status zr_hash_index_sets(int64_t dense_size, int32_t n_parts, uint64_t part_
                                static_cast<cudaStream_t>(stream));
 }
 
+size_t zr_hash_directory_size(int64_t dense_size, int32_t n_parts) {
+  if (dense_size < 1 || dense_size > INT32_MAX || n_parts < 1 || n_parts > ZR_MAX_PARTS) return 0;
+  return zr::hash_directory_bytes(dense_size, n_parts);
+}
+
+zr_status zr_hash_directory(int64_t dense_size, int32_t n_parts, uint64_t part_seed,
+                            int32_t* d_dir, size_t dir_bytes, void* stream) {
+  if (dense_size < 1 || dense_size > INT32_MAX || n_parts < 1 || n_parts > ZR_MAX_PARTS || !d_dir)
+    return ZR_ERR_INVALID_ARG;
+  zr_status st = zr::check_ws(d_dir, dir_bytes, zr::hash_directory_bytes(dense_size, n_parts));
+  if (st != ZR_OK) return st;
+  return zr::hash_directory_launch(dense_size, n_parts, part_seed, d_dir,
+                                   static_cast<cudaStream_t>(stream));
+}
+
 size_t zr_hash_bitmap_workspace_size(int64_t dense_size, int32_t n_parts) {
   if (dense_size < 1 || dense_size > INT32_MAX || n_parts < 1 || n_parts > ZR_MAX_PARTS) return 0;
   return zr::hash_bitmap_workspace_bytes(dense_size, n_parts);
 }
 
-zr_status zr_hash_bitmap_encode(const int32_t* sets, const int64_t* d_set_offsets,
-                                int64_t dense_size, int32_t n_parts, const int32_t* keys,
-                                int64_t n_keys, uint32_t* out_bits, int64_t out_cap_words,
+zr_status zr_hash_bitmap_encode(const int32_t* d_dir, int64_t dense_size, int32_t n_parts,
+                                uint64_t part_seed, const int32_t* keys, int64_t n_keys,
+                                uint32_t* out_bits, int64_t out_cap_words,
                                 int64_t* d_word_offsets, void* ws, size_t ws_bytes, void* stream) {
   if (dense_size < 1 || dense_size > INT32_MAX || n_parts < 1 || n_parts > ZR_MAX_PARTS)
     return ZR_ERR_INVALID_ARG;
-  if (!sets || !d_set_offsets || !out_bits || !d_word_offsets || n_keys < 0 ||
-      (n_keys > 0 && !keys))
+  if (!d_dir || !out_bits || !d_word_offsets || n_keys < 0 || (n_keys > 0 && !keys))
     return ZR_ERR_INVALID_ARG;
   if (out_cap_words < (dense_size + 31) / 32 + n_parts) return ZR_ERR_CAPACITY;
   zr_status st = zr::check_ws(ws, ws_bytes, zr::hash_bitmap_workspace_bytes(dense_size, n_parts));
   if (st != ZR_OK) return st;
-  return zr::hash_bitmap_encode_launch(sets, d_set_offsets, dense_size, n_parts, keys, n_keys,
+  return zr::hash_bitmap_encode_launch(d_dir, dense_size, n_parts, part_seed, keys, n_keys,
                                        out_bits, out_cap_words, d_word_offsets, ws,
                                        static_cast<cudaStream_t>(stream));
 }
 
-zr_status zr_hash_bitmap_decode(const int32_t* sets, const int64_t* d_set_offsets,
-                                int64_t dense_size, int32_t n_parts, const uint32_t* bits,
-                                int32_t* out_keys, int64_t out_cap, int64_t* d_key_offsets,
-                                void* ws, size_t ws_bytes, void* stream) {
+zr_status zr_hash_bitmap_decode(const int32_t* d_dir, int64_t dense_size, int32_t n_parts,
+                                uint64_t part_seed, const uint32_t* bits, int32_t* out_keys,
+                                int64_t out_cap, int64_t* d_key_offsets, void* ws,
+                                size_t ws_bytes, void* stream) {
   if (dense_size < 1 || dense_size > INT32_MAX || n_parts < 1 || n_parts > ZR_MAX_PARTS)
     return ZR_ERR_INVALID_ARG;
-  if (!sets || !d_set_offsets || !bits || !d_key_offsets || out_cap < 0 || (out_cap > 0 && !out_keys))
+  if (!d_dir || !bits || !d_key_offsets || out_cap < 0 || (out_cap > 0 && !out_keys))
     return ZR_ERR_INVALID_ARG;
   zr_status st = zr::check_ws(ws, ws_bytes, zr::hash_bitmap_workspace_bytes(dense_size, n_parts));
   if (st != ZR_OK) return st;
-  return zr::hash_bitmap_decode_launch(sets, d_set_offsets, dense_size, n_parts, bits, out_keys,
+  return zr::hash_bitmap_decode_launch(d_dir, dense_size, n_parts, part_seed, bits, out_keys,
                                        out_cap, d_key_offsets, ws,
                                        static_cast<cudaStream_t>(stream));
 }

@@ -39,14 +39,18 @@ zr_status densify_launch(const int32_t* const* idx, const int64_t* nnz, int n, i
 zr_status index_sets_launch(int64_t m, int n_parts, uint64_t part_seed, int32_t* out_sets,
                             int64_t* d_offsets, void* ws, cudaStream_t stream);
 
-// Hash bitmap encode / decode; arguments already validated.
+// Zen's directory of index-set counts and the hash bitmap encode / decode;
+// arguments already validated.
+size_t hash_directory_bytes(int64_t m, int n_parts);
+zr_status hash_directory_launch(int64_t m, int n_parts, uint64_t part_seed, int32_t* d_dir,
+                                cudaStream_t stream);
 size_t hash_bitmap_workspace_bytes(int64_t m, int n_parts);
-zr_status hash_bitmap_encode_launch(const int32_t* sets, const int64_t* d_set_offsets, int64_t m,
-                                    int n_parts, const int32_t* keys, int64_t n_keys,
+zr_status hash_bitmap_encode_launch(const int32_t* d_dir, int64_t m, int n_parts,
+                                    uint64_t part_seed, const int32_t* keys, int64_t n_keys,
                                     uint32_t* out_bits, int64_t out_cap_words,
                                     int64_t* d_word_offsets, void* ws, cudaStream_t stream);
-zr_status hash_bitmap_decode_launch(const int32_t* sets, const int64_t* d_set_offsets, int64_t m,
-                                    int n_parts, const uint32_t* bits, int32_t* out_keys,
+zr_status hash_bitmap_decode_launch(const int32_t* d_dir, int64_t m, int n_parts,
+                                    uint64_t part_seed, const uint32_t* bits, int32_t* out_keys,
                                     int64_t out_cap, int64_t* d_key_offsets, void* ws,
                                     cudaStream_t stream);
 

@@ -290,12 +290,41 @@ zr_status zr_hash_index_sets(int64_t dense_size, int32_t n_parts, uint64_t part_
                              void* stream);
 
 /*
+ * Zen's index sets as a directory [ZEN section 3.3.2 "Hash bitmap":
+ * I_p = {x in [0, M) : h0(x) = p}, ascending, fixed for the whole run].  The
+ * hash bitmap calls below use this directory instead of the index sets; it
+ * is built once per (M, n_parts, part_seed), in two launches, and holds
+ * NB = ceil(log2 n_parts) bits per index instead of the index sets' 32.
+ *
+ * dense_size M, 1 <= M <= 2^31 - 1.   n_parts: 1 <= n_parts <= ZR_MAX_PARTS.
+ * d_dir      device buffer of zr_hash_directory_size(M, n_parts) bytes,
+ *            16-byte aligned.  With R = ceil(M / ZR_HASH_RANGE) and S = R + 1
+ *            rounded up to a multiple of 4, it holds
+ *            header  256 bytes: int64 magic, M, n_parts, part_seed;
+ *            counts  int32, from byte 256: entry [p S + r], r <= R, is
+ *                    |{x < min(r ZR_HASH_RANGE, M) : h0(x) = p}|, so entry
+ *                    [p S + R] is |I_p|;
+ *            slices  uint64, from byte 256 + ceil(n_parts S 4 / 256) 256:
+ *                    word [(r NB + b) 32 + l] has bit k set iff bit b of
+ *                    h0(r ZR_HASH_RANGE + 64 l + k) is set (bits of indices
+ *                    at or past M unspecified).
+ *            The encode and decode calls read it; they report
+ *            ZR_ERR_INVALID_ARG, and write nothing, for a directory built
+ *            for another (M, n_parts, part_seed), and they check every
+ *            range's counts against the slices.
+ * h0 is the partition hash of zr_sparse_aggregate (same part_seed).
+ */
+#define ZR_HASH_RANGE 2048
+size_t zr_hash_directory_size(int64_t dense_size, int32_t n_parts);
+zr_status zr_hash_directory(int64_t dense_size, int32_t n_parts, uint64_t part_seed,
+                            int32_t* d_dir, size_t dir_bytes, void* stream);
+
+/*
  * Hash bitmap encode [ZEN section 3.3.2, Figure 10, Algorithm 2
  * hash_bitmap_encode: a server marks which elements of I_p are nonzero,
  * one bit each, so that all servers' bitmaps total |G| bits].
  *
- * sets, d_set_offsets  the index sets from zr_hash_index_sets (device).
- * dense_size, n_parts  as there.
+ * d_dir                 the directory of (dense_size, n_parts, part_seed).
  * keys, n_keys   device int32: the nonzero indices (any order, each in
  *                [0, M)), e.g. the out_idx of zr_sparse_aggregate.
  * out_bits       device uint32[out_cap_words], out_cap_words >=
@@ -307,12 +336,12 @@ zr_status zr_hash_index_sets(int64_t dense_size, int32_t n_parts, uint64_t part_
  * ws             device workspace of zr_hash_bitmap_workspace_size(M,
  *                n_parts) bytes, 16-byte aligned; its first 4 bytes are the
  *                status word (ZR_ERR_INPUT_UNSORTED: a key outside [0, M);
- *                ZR_ERR_INVALID_ARG: offsets or sets that are not index sets
- *                of [0, M)).
+ *                ZR_ERR_INVALID_ARG: a directory that does not match h0).
+ * Four launches: two memsets, the membership marks, the encode.
  */
-zr_status zr_hash_bitmap_encode(const int32_t* sets, const int64_t* d_set_offsets,
-                                int64_t dense_size, int32_t n_parts, const int32_t* keys,
-                                int64_t n_keys, uint32_t* out_bits, int64_t out_cap_words,
+zr_status zr_hash_bitmap_encode(const int32_t* d_dir, int64_t dense_size, int32_t n_parts,
+                                uint64_t part_seed, const int32_t* keys, int64_t n_keys,
+                                uint32_t* out_bits, int64_t out_cap_words,
                                 int64_t* d_word_offsets, void* ws, size_t ws_bytes, void* stream);
 
 /*
@@ -320,23 +349,29 @@ zr_status zr_hash_bitmap_encode(const int32_t* sets, const int64_t* d_set_offset
  * worker maps the set bits j of server p's bitmap back to the indices
  * I_p[j]].
  *
+ * d_dir          the directory of (dense_size, n_parts, part_seed).
  * bits           device uint32 bitmaps laid out as zr_hash_bitmap_encode
- *                writes them (partition p from word sum_{q<p} ceil(|I_q|/32)).
+ *                writes them (partition p from word sum_{q<p} ceil(|I_q|/32));
+ *                the buffer holds at least the sum_q ceil(|I_q|/32) words the
+ *                directory gives (ceil(M / 32) + n_parts always suffices).
  * out_keys       device int32[out_cap]: partition-major, ascending inside a
  *                partition (the indices I_p[j] of the set bits j).
  * d_key_offsets  device int64[n_parts + 1] (output): partition p's keys are
  *                out_keys[d_key_offsets[p] .. d_key_offsets[p+1]).
  * ws             as for encode.  Status: ZR_ERR_CAPACITY if more keys than
  *                out_cap (nothing is written past it), ZR_ERR_INVALID_ARG if a
- *                padding bit is set or the sets are not index sets of [0, M).
+ *                padding bit is set or the directory does not match h0.
+ * Four launches: the status memset, the segment counts, their scan, the
+ * decode.
  */
-zr_status zr_hash_bitmap_decode(const int32_t* sets, const int64_t* d_set_offsets,
-                                int64_t dense_size, int32_t n_parts, const uint32_t* bits,
-                                int32_t* out_keys, int64_t out_cap, int64_t* d_key_offsets,
-                                void* ws, size_t ws_bytes, void* stream);
+zr_status zr_hash_bitmap_decode(const int32_t* d_dir, int64_t dense_size, int32_t n_parts,
+                                uint64_t part_seed, const uint32_t* bits, int32_t* out_keys,
+                                int64_t out_cap, int64_t* d_key_offsets, void* ws,
+                                size_t ws_bytes, void* stream);
 
 /* Workspace bytes zr_hash_bitmap_encode / _decode need (0 on invalid
- * arguments). */
+ * arguments): the status word, an M-bit membership map and 4 bytes per
+ * partition per ZR_HASH_RANGE indices. */
 size_t zr_hash_bitmap_workspace_size(int64_t dense_size, int32_t n_parts);
 
 /*

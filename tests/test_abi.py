@@ -222,3 +222,43 @@ def test_densification_argument_errors_before_launch(zr):
     assert call(nnz=[3, 4, 5, 2000]) == zr.ZR_ERR_INVALID_ARG
     assert call(ws=p + 8) == zr.ZR_ERR_ALIGNMENT
     assert call(ws_bytes=ws - 1) == zr.ZR_ERR_CAPACITY
+
+
+def test_hash_bitmap_sizes_and_argument_errors_before_launch(zr):
+    hdr = open(os.path.join(ROOT, "include", "zr.h")).read()
+    m = re.search(r"#define ZR_HASH_RANGE (\d+)", hdr)
+    assert m and zr.ZR_HASH_RANGE == int(m.group(1))
+    rng = zr.ZR_HASH_RANGE
+    for dense, parts in ((1, 1), (rng, 8), (rng + 1, 8), ((1 << 25), 16), ((1 << 31) - 1, 256)):
+        ranges = -(-dense // rng)
+        stride = (ranges + 1 + 3) // 4 * 4
+        nb = max(0, (parts - 1).bit_length())
+        counts = -(-(parts * stride * 4) // 256) * 256
+        assert zr.zr_hash_directory_size(dense, parts) == 256 + counts + ranges * nb * 32 * 8
+        assert zr.zr_hash_bitmap_workspace_size(dense, parts) > 0
+    for bad in ((0, 8), ((1 << 31), 8), (100, 0), (100, zr.ZR_MAX_PARTS + 1)):
+        assert zr.zr_hash_directory_size(*bad) == 0
+        assert zr.zr_hash_bitmap_workspace_size(*bad) == 0
+    p = 1 << 40
+    dsz = zr.zr_hash_directory_size(1000, 4)
+    assert zr.zr_hash_directory(1000, 4, 0, None, dsz, None) == zr.ZR_ERR_INVALID_ARG
+    assert zr.zr_hash_directory(1000, 4, 0, p + 4, dsz, None) == zr.ZR_ERR_ALIGNMENT
+    assert zr.zr_hash_directory(1000, 4, 0, p, dsz - 1, None) == zr.ZR_ERR_CAPACITY
+    ws = zr.zr_hash_bitmap_workspace_size(1000, 4)
+    cap = (1000 + 31) // 32 + 4
+    enc = lambda **kw: zr.zr_hash_bitmap_encode(  # noqa: E731
+        kw.get("dir", p), 1000, 4, 0, kw.get("keys", p), kw.get("n_keys", 10), p,
+        kw.get("cap", cap), p, kw.get("ws", p), kw.get("ws_bytes", ws), None)
+    assert enc(dir=None) == zr.ZR_ERR_INVALID_ARG
+    assert enc(keys=None) == zr.ZR_ERR_INVALID_ARG
+    assert enc(n_keys=-1) == zr.ZR_ERR_INVALID_ARG
+    assert enc(cap=cap - 1) == zr.ZR_ERR_CAPACITY
+    assert enc(ws=p + 8) == zr.ZR_ERR_ALIGNMENT
+    assert enc(ws_bytes=ws - 1) == zr.ZR_ERR_CAPACITY
+    dec = lambda **kw: zr.zr_hash_bitmap_decode(  # noqa: E731
+        kw.get("dir", p), 1000, 4, 0, p, kw.get("out", p), kw.get("cap", 10), p, p,
+        kw.get("ws_bytes", ws), None)
+    assert dec(dir=None) == zr.ZR_ERR_INVALID_ARG
+    assert dec(out=None) == zr.ZR_ERR_INVALID_ARG
+    assert dec(cap=-1) == zr.ZR_ERR_INVALID_ARG
+    assert dec(ws_bytes=ws - 1) == zr.ZR_ERR_CAPACITY

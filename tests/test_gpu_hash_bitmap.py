@@ -1,5 +1,6 @@
-"""GPU parity: Zen's index sets and hash bitmap encode / decode (through the
-C ABI) against the CPU oracle, bit for bit; the C4 union at full size."""
+"""GPU parity: Zen's hash bitmap encode / decode and the directory of
+index-set counts they use (through the C ABI) against the CPU oracle, bit
+for bit; the index sets themselves; the C4 union at full size."""
 
 import numpy as np
 import pytest
@@ -17,11 +18,56 @@ def env():
     return require_cuda()
 
 
+def directory_want(m, parts, seed, rng_keys):
+    """The directory from its definition: row p, column r counts the
+    indices x < min(r * range, M) with h0(x) = p."""
+    p = osp.h0(np.arange(m, dtype=np.int64), parts, seed)
+    R = -(-m // rng_keys)
+    want = np.zeros((parts, R + 1), dtype=np.int64)
+    for r in range(R):
+        blk = p[r * rng_keys:(r + 1) * rng_keys]
+        want[:, r + 1] = want[:, r] + np.bincount(blk, minlength=parts)
+    return want
+
+
+def dir_counts(hb, m, parts, rng_keys):
+    """The directory's count rows (row stride R + 1 rounded up to 4)."""
+    R = -(-m // rng_keys)
+    stride = (R + 1 + 3) // 4 * 4
+    return hb.directory[64: 64 + parts * stride].view(parts, stride)[:, : R + 1]
+
+
+def slices_want(m, parts, seed, rng_keys):
+    """The directory's slices from their definition: word (r, b, lane) has
+    bit k set iff bit b of h0(r * range + 64 * lane + k) is (indices at or
+    past M count as 0)."""
+    nb = max(0, (parts - 1).bit_length())
+    R = -(-m // rng_keys)
+    p = np.zeros(R * rng_keys, dtype=np.uint64)
+    p[:m] = osp.h0(np.arange(m, dtype=np.int64), parts, seed)
+    p = p.reshape(R, 32, 64)
+    out = np.zeros((R, nb, 32), dtype=np.uint64)
+    for b in range(nb):
+        bits = (p >> np.uint64(b)) & np.uint64(1)
+        out[:, b, :] = (bits << np.arange(64, dtype=np.uint64)).sum(axis=2, dtype=np.uint64)
+    return out
+
+
 def check(torch, zr, m, parts, seed, keys):
     hb = zr.HashBitmap(m, parts, seed)
-    sets, off = ohb.index_sets(m, parts, seed)
-    assert np.array_equal(hb.sets.cpu().numpy(), sets)
-    assert np.array_equal(hb.offsets.cpu().numpy(), off)
+    rk = zr.ZR_HASH_RANGE
+    got = dir_counts(hb, m, parts, rk).cpu().numpy()
+    assert np.array_equal(got, directory_want(m, parts, seed, rk))
+    R = -(-m // rk)
+    counts_bytes = -(-(parts * ((R + 1 + 3) // 4 * 4) * 4) // 256) * 256
+    sl = hb.directory.cpu().numpy().view(np.uint8)[256 + counts_bytes:].view(np.uint64)
+    want_sl = slices_want(m, parts, seed, rk)
+    # bits of indices past M are unspecified in the last lanes: compare below M
+    valid = np.zeros(R * rk, dtype=bool)
+    valid[:m] = True
+    vmask = (valid.reshape(R, 32, 64).astype(np.uint64) << np.arange(64, dtype=np.uint64)).sum(
+        axis=2, dtype=np.uint64)
+    assert np.array_equal(sl.reshape(want_sl.shape) & vmask[:, None, :], want_sl & vmask[:, None, :])
     d_keys = torch.from_numpy(np.ascontiguousarray(keys, dtype=np.int32)).cuda()
     bits, woff = hb.encode(d_keys)
     torch.cuda.synchronize()
@@ -41,14 +87,24 @@ def check(torch, zr, m, parts, seed, keys):
     return hb
 
 
-@pytest.mark.parametrize("parts", [1, 3, 8, 16, 64, 256])
+@pytest.mark.parametrize("parts", [1, 2, 3, 8, 16, 17, 32, 64, 200, 256])
 def test_small_and_ragged(env, parts):
     torch, zr = env
     rng = np.random.default_rng(parts)
-    for m in (1, 15, 33, 1000, 100_003):
+    # sizes below one lane, one range, ragged ranges and several ranges
+    for m in (1, 15, 33, 64, 1000, 2048, 2049, 100_003):
         for density in (0.0, 0.3, 1.0):
             keys = np.nonzero(rng.random(m) < density)[0].astype(np.int32)
             check(torch, zr, m, parts, int(rng.integers(0, 1 << 62)), rng.permutation(keys))
+
+
+def test_index_sets(env):
+    torch, zr = env
+    for m, parts, seed in ((1, 1, 0), (1000, 3, 5), (100_003, 8, 7), (50_000, 256, 9)):
+        sets, off = zr.hash_index_sets(m, parts, seed)
+        want_sets, want_off = ohb.index_sets(m, parts, seed)
+        assert np.array_equal(sets.cpu().numpy(), want_sets)
+        assert np.array_equal(off.cpu().numpy(), want_off)
 
 
 def test_union_keys_round_trip_c4(env):
@@ -75,8 +131,53 @@ def test_status_errors(env):
     assert hb.status() == zr.ZR_ERR_INPUT_UNSORTED
     keys = torch.arange(0, 1000, 2, dtype=torch.int32, device="cuda")
     bits, _ = hb.encode(keys)
-    small = torch.full((10,), -1, dtype=torch.int32, device="cuda")
+    big = torch.full((600,), -1, dtype=torch.int32, device="cuda")
     koff = torch.empty(5, dtype=torch.int64, device="cuda")
-    hb.decode(bits, small, koff)
+    hb.decode(bits, big[:10], koff)
     torch.cuda.synchronize()
     assert hb.status() == zr.ZR_ERR_CAPACITY
+    # nothing is written past the capacity
+    assert bool((big[10:] == -1).all())
+
+
+def test_padding_bit_and_foreign_directory(env):
+    torch, zr = env
+    m, parts = 5000, 3
+    # a seed whose partition 0 ends inside a word
+    seed = next(sd for sd in range(100) if ohb.index_sets(m, parts, sd)[1][1] % 32)
+    hb = zr.HashBitmap(m, parts, seed)
+    keys = torch.arange(0, m, 3, dtype=torch.int32, device="cuda")
+    bits, woff = hb.encode(keys)
+    torch.cuda.synchronize()
+    out = torch.empty(m, dtype=torch.int32, device="cuda")
+    koff = torch.empty(parts + 1, dtype=torch.int64, device="cuda")
+    # a set padding bit past the end of partition 0's set
+    w = woff.cpu().numpy()
+    n0 = int(dir_counts(hb, m, parts, zr.ZR_HASH_RANGE)[0, -1])
+    assert n0 % 32, "partition 0 must end inside a word for this case"
+    bad = bits.clone()
+    bad[int(w[1]) - 1] |= -(1 << 31)  # bit 31
+    hb.decode(bad, out, koff)
+    torch.cuda.synchronize()
+    assert hb.status() == zr.ZR_ERR_INVALID_ARG
+    # a directory built for another seed: every call reports it, and writes
+    # stay inside the given buffers
+    other = zr.HashBitmap(m, parts, seed + 1)
+    hb.directory, saved = other.directory, hb.directory
+    hb.encode(keys)
+    torch.cuda.synchronize()
+    assert hb.status() == zr.ZR_ERR_INVALID_ARG
+    hb.decode(bits, out, koff)
+    torch.cuda.synchronize()
+    assert hb.status() == zr.ZR_ERR_INVALID_ARG
+    # lengths that do not add up to M
+    broken = saved.clone()
+    hb.directory = broken
+    dir_counts(hb, m, parts, zr.ZR_HASH_RANGE)[0, -1] += 1
+    hb.encode(keys)
+    torch.cuda.synchronize()
+    assert hb.status() == zr.ZR_ERR_INVALID_ARG
+    hb.directory = saved
+    hb.encode(keys)
+    torch.cuda.synchronize()
+    assert hb.status() == zr.ZR_OK
