@@ -335,8 +335,8 @@ hb_dir_build_kernel(const HbGeom G, long long* hdr, int32_t* cnt, uint64_t* sl) 
 
 // In place, one CTA per row: entries 0 .. n-1 of row q (rows `stride` ints
 // apart, 16-byte aligned) become their exclusive prefix sum, so the last
-// entry ends as the row total.  16 entries per thread per pass.
-constexpr int kScanPer = 16;
+// entry ends as the row total.  32 entries per thread per pass.
+constexpr int kScanPer = 32;
 
 __global__ void __launch_bounds__(kScanThreads) hb_scan_kernel(int32_t* a, int n, int stride) {
   __shared__ int32_t s_warp[kScanThreads / 32];
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kThreads) hb_encode_kernel(const __grid_consta
     if (blockIdx.x == 0 && threadIdx.x == 0) flag(A.status, ZR_ERR_CAPACITY);
     return;
   }
-  const int mwords = (G.m + 31) >> 5;
+  const int mwords = (int)(((long long)G.m + 31) >> 5);  // M + 31 can pass 2^31 - 1
   for (int r = blockIdx.x * kWarps + warp; r < G.ranges; r += gridDim.x * kWarps) {
     const int x0 = r * kRangeKeys + lane * kLaneKeys;
     const RowCache c_s = row_cache(G, A.cnt, r), c_e = row_cache(G, A.cnt, r + 1);
@@ -534,8 +534,9 @@ __global__ void __launch_bounds__(kThreads) hb_encode_kernel(const __grid_consta
 
 // ---------------------------------------------------------------- decode
 // seg[q][r] = set bits of partition q's bitmap in range r's segment
-// [cnt[q][r], cnt[q][r+1]); seg[q][R] = 0.  A warp per range, its lanes over
-// the segment's words.  CTA 0 also checks that no padding bit is set.
+// [cnt[q][r], cnt[q][r+1]); seg[q][R] = 0.  A warp per range, a lane per
+// partition, each lane over its segment's words (four loads in flight).
+// CTA 0 also checks that no padding bit is set.
 __global__ void __launch_bounds__(kThreads)
 hb_seg_count_kernel(const HbGeom G, const long long* hdr, const int32_t* cnt,
                     const uint32_t* bits, int32_t* seg, int32_t* status) {
@@ -555,27 +556,30 @@ hb_seg_count_kernel(const HbGeom G, const long long* hdr, const int32_t* cnt,
     }
   }
   for (int r = blockIdx.x * kWarps + (threadIdx.x >> 5); r < G.ranges; r += gridDim.x * kWarps) {
-    const RowCache c_s = row_cache(G, cnt, r), c_e = row_cache(G, cnt, r + 1);
-    for (int q = 0; q < G.parts; ++q) {
-      const int s = row_get(G, cnt, c_s, q, r);
-      const int e = row_get(G, cnt, c_e, q, r + 1);
+    for (int q = lane; q < G.parts; q += 32) {
+      const int s = __ldg(cnt + (size_t)q * G.stride + r);
+      const int e = __ldg(cnt + (size_t)q * G.stride + r + 1);
       uint32_t c = 0;
       if (s >= 0 && e >= s && e <= s_len[q]) {
         if (e > s) {
           const uint32_t lo = s_woff[q] * 32u + (uint32_t)s, hi = s_woff[q] * 32u + (uint32_t)e;
           const uint32_t w0 = lo >> 5, w1 = (hi - 1u) >> 5;
-          for (uint32_t w = w0 + lane; w <= w1; w += 32) {
-            uint32_t x = __ldg(bits + w);
-            if (w == w0) x &= ~0u << (lo & 31u);
-            if (w == w1 && (hi & 31u)) x &= ~0u >> (32u - (hi & 31u));
-            c += __popc(x);
+          for (uint32_t w = w0; w <= w1; w += 4) {
+            uint32_t x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) x[u] = w + u <= w1 ? __ldg(bits + w + u) : 0u;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (w + u == w0) x[u] &= ~0u << (lo & 31u);
+              if (w + u == w1 && (hi & 31u)) x[u] &= ~0u >> (32u - (hi & 31u));
+              c += __popc(x[u]);
+            }
           }
         }
-      } else if (lane == 0) {
+      } else {
         flag(status, ZR_ERR_INVALID_ARG);
       }
-      c = warp_sum_u32(c);
-      if (lane == 0) seg[(size_t)q * G.stride + r] = (int32_t)c;
+      seg[(size_t)q * G.stride + r] = (int32_t)c;
     }
   }
 }
@@ -733,6 +737,7 @@ __global__ void __launch_bounds__(kThreads, 8) hb_decode_kernel(const __grid_con
           const int kp = select64(s_eq[warp][qi][l], rb);
           const long long o = s_ob[warp][qi] + jj;
           if (o < A.out_cap) A.out[o] = r * kRangeKeys + l * kLaneKeys + kp;
+          else flag(A.status, s_koff[G.parts] > A.out_cap ? ZR_ERR_CAPACITY : ZR_ERR_INTERNAL);
         }
       }
       __syncwarp();

@@ -181,3 +181,40 @@ def test_padding_bit_and_foreign_directory(env):
     hb.encode(keys)
     torch.cuda.synchronize()
     assert hb.status() == zr.ZR_OK
+
+
+def test_maximum_size_round_trip(env):
+    """M = 2^31 - 1 and 256 partitions (the largest request: a 3 GB
+    directory, 2^20 ranges, the last one ragged).  Properties that hold at
+    any size: the directory's lengths are the partition sizes of h0 (their
+    sum is M), and decode(encode(keys)) is the keys grouped by h0 and
+    ascending inside each partition."""
+    torch, zr = env
+    m, parts, seed = (1 << 31) - 1, zr.ZR_MAX_PARTS, 77
+    rng = np.random.default_rng(5)
+    keys = np.unique(np.concatenate([
+        rng.integers(0, m, size=200_000, dtype=np.int64),
+        np.array([0, 1, 2047, 2048, m - 2048, m - 2, m - 1], dtype=np.int64)])).astype(np.int32)
+    hb = zr.HashBitmap(m, parts, seed)
+    lengths = dir_counts(hb, m, parts, zr.ZR_HASH_RANGE)[:, -1].cpu().numpy()
+    assert int(lengths.sum()) == m and lengths.min() > 0
+    bits, woff = hb.encode(torch.from_numpy(rng.permutation(keys)).cuda())
+    torch.cuda.synchronize()
+    assert hb.status() == zr.ZR_OK
+    w = woff.cpu().numpy()
+    assert np.array_equal(np.diff(w), (lengths + 31) // 32)
+    out = torch.full((keys.size,), -1, dtype=torch.int32, device="cuda")
+    koff = torch.empty(parts + 1, dtype=torch.int64, device="cuda")
+    hb.decode(bits, out, koff)
+    torch.cuda.synchronize()
+    assert hb.status() == zr.ZR_OK
+    p = osp.h0(keys.astype(np.int64), parts, seed)
+    order = np.lexsort((keys, p))
+    assert np.array_equal(out.cpu().numpy(), keys[order])
+    want_koff = np.zeros(parts + 1, dtype=np.int64)
+    want_koff[1:] = np.cumsum(np.bincount(p, minlength=parts))
+    assert np.array_equal(koff.cpu().numpy(), want_koff)
+    # the set bits total the keys
+    ones = np.array([bin(i).count("1") for i in range(256)], dtype=np.int64)
+    words = bits[: int(w[-1])].cpu().numpy().view(np.uint8)
+    assert int(ones[words].sum()) == keys.size
