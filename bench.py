@@ -481,9 +481,9 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
             del dn
         if wanted(sel, "next_c4_hb"):
             # Zen's Pull: hash bitmaps of the union's keys over M = 2^25.  The
-            # encode / decode recompute h0 for all M indices (bound by that
-            # arithmetic: hashes_per_s); their bytes are the keys and the
-            # bitmaps.
+            # encode / decode go over all M indices through the directory's
+            # slices (bound by that arithmetic: indices_per_s); their bytes are
+            # the keys and the bitmaps.
             hb = zr.HashBitmap(m, P, seed)
             keys = d_sets[0][2].out_idx[:union]
             hb.encode(keys)
@@ -496,13 +496,13 @@ def run_parts(torch, zr, dev, sel, steps, warmup, peak, clock_off):
             ms = time_calls(torch, [lambda i: zr.zr_hash_directory(
                 m, P, seed, hb.directory.data_ptr(), dir_bytes, stream)], steps, warmup)
             parts["next_c4_hb_directory"] = part_entry(dir_bytes, ms, peak,
-                                                       hashes_per_s=m / (ms / 1e3))
+                                                       indices_per_s=m / (ms / 1e3))
             ms = time_calls(torch, [lambda i: hb.encode(keys)], steps, warmup)
             parts["next_c4_hb_encode"] = part_entry(union * 4 + words * 4 + (P + 1) * 8, ms, peak,
-                                                    hashes_per_s=m / (ms / 1e3))
+                                                    indices_per_s=m / (ms / 1e3))
             ms = time_calls(torch, [lambda i: hb.decode(hb_bits, hb_out, hb_koff)], steps, warmup)
             parts["next_c4_hb_decode"] = part_entry(words * 4 + union * 4 + (P + 1) * 8, ms, peak,
-                                                    hashes_per_s=m / (ms / 1e3))
+                                                    indices_per_s=m / (ms / 1e3))
             sets = torch.empty(m, dtype=torch.int32, device=dev)
             offs = torch.empty(P + 1, dtype=torch.int64, device=dev)
             sets_ws = torch.empty(zr.zr_partition_workspace_size(m, P), dtype=torch.uint8,
