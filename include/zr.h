@@ -25,11 +25,13 @@
  *     (an unsorted or out-of-range sparse index) are written to a status
  *     word inside `ws`; read it with zr_query_status after the stream work.
  *   - zr_partition, zr_partition_static and zr_hash_index_sets are each one
- *     cooperative launch whose CTAs wait for one another once.  That wait is bounded: if the CTAs cannot all run at
- *     once (for example while another cooperative grid holds the device from
- *     a stream that is not ordered with this one) it gives up after about a
- *     second, the status word becomes ZR_ERR_TIMEOUT and the outputs are
- *     unspecified.  Order such calls on one stream, or with events.
+ *     cooperative launch whose CTAs wait for one another once.  That wait is
+ *     bounded: if the CTAs cannot all run at once (for example while another
+ *     cooperative grid holds the device from a stream that is not ordered
+ *     with this one) it gives up after about a second, the status word
+ *     becomes ZR_ERR_TIMEOUT and the outputs are unspecified.  Order such
+ *     calls on one stream, or with events.  No other kernel waits on
+ *     another CTA.
  *   - No C++ exception crosses this interface.
  */
 #ifndef ZR_H
