@@ -266,53 +266,50 @@ __device__ __forceinline__ int rank_get(const int (&v)[2], int r) {
 }
 
 // Walks the bin rank by rank, lowest rank first, in chunks of up to 32
-// consecutive entries of one rank: lane l takes entry 32c + l of chunk c of
-// its rank.  The loads of kChunks chunks are issued together (load(t, rank,
-// pos) fills slot t), then apply(t, ok) runs for the chunks in order, ok
-// saying whether the lane holds an entry.  A list is strictly ascending, so
-// the keys of one chunk are distinct and a chunk is applied at once; chunks
-// go in rank order, so a key held by several ranks meets the lowest rank
-// first.  Rank r's chunks are numbers [cp_r, cp_r + nc_r) of the bin; the
-// rank of chunk j is the number of ranks whose chunks end at or before j,
-// one ballot, so the walk has no data-dependent branch.
+// consecutive entries of one rank: lane l takes entry c + l of the rank's
+// chunk at entry offset c.  The loads of kChunks chunks are issued together
+// (load(t, rank, pos) fills slot t), then apply(t, ok) runs for the chunks
+// in order, ok saying whether the lane holds an entry.  A list is strictly
+// ascending, so the keys of one chunk are distinct and a chunk is applied
+// at once; chunks go in rank order, so a key held by several ranks meets
+// the lowest rank first.  The cursor (rank, its first position and count,
+// the next chunk's offset) is the same on every lane, so the walk's
+// branches and the shuffles that fetch the next rank's row are uniform.
 template <int kChunks, typename Load, typename Apply>
 __device__ __forceinline__ void walk_bin(const BinRows& R, int n, Load&& load, Apply&& apply) {
   const int lane = threadIdx.x & 31;
-  int cp[2], cend[2];
-  int carry = 0;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int nc = (R.len[h] + 31) >> 5;
-    const int incl = warp_incl_scan(nc);
-    cp[h] = carry + incl - nc;
-    cend[h] = carry + incl;
-    carry += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  const int chunks = carry;
-  const bool live0 = lane < n, live1 = lane + 32 < n;
-  for (int j0 = 0; j0 < chunks; j0 += kChunks) {
+  int r = -1, lo = 0, len = 0, c = 0;
+  auto advance = [&]() {
+    for (++r; r < n; ++r) {
+      len = rank_get(R.len, r);
+      if (len > 0) {
+        lo = rank_get(R.lo, r);
+        c = 0;
+        return;
+      }
+    }
+  };
+  advance();
+  while (r < n) {
     bool ok[kChunks];
+    int got = 0;
 #pragma unroll
     for (int t = 0; t < kChunks; ++t) {
-      const int j = j0 + t;
       ok[t] = false;
-      if (j < chunks) {
-        int r = __popc(__ballot_sync(0xffffffffu, live0 && cend[0] <= j));
-        if (n > 32) r += __popc(__ballot_sync(0xffffffffu, live1 && cend[1] <= j));
-        // every lane takes part in the shuffles, then the lanes past the
-        // rank's end load nothing
-        const int i = ((j - rank_get(cp, r)) << 5) + lane;
-        const int len = rank_get(R.len, r);
-        const int lo = rank_get(R.lo, r);
+      if (r < n) {
+        const int i = c + lane;
         if (i < len) {
           ok[t] = true;
           load(t, r, lo + i);
         }
+        c += 32;
+        if (c >= len) advance();
+        got = t + 1;
       }
     }
 #pragma unroll
     for (int t = 0; t < kChunks; ++t) {
-      if (j0 + t < chunks) {
+      if (t < got) {
         apply(t, ok[t]);
         __syncwarp();
       }
