@@ -19,11 +19,12 @@
 //   3. scan:    one CTA per partition turns the per-bin counts into each
 //      bin's first output position in that partition.
 //   4. write:   per bin, a warp walks the bin rank by rank in chunks of up
-//      to 32 consecutive entries of one rank (the loads of 8 chunks in
-//      flight; one ballot gives each chunk's rank), or, where bins hold few
-//      entries, flattened in groups of 32 across rank boundaries applied in
-//      ascending runs, and folds them into a warp-private W-float window in
-//      ascending rank order, which is the left fold of the holders' values.  Then the members are placed into
+//      to 32 consecutive entries of one rank (the loads of 12 chunks in
+//      flight; a warp-uniform cursor gives each chunk's rank), or, where
+//      bins hold few entries, flattened in groups of 32 across rank
+//      boundaries applied in ascending runs, and folds them into a
+//      warp-private W-float window in ascending rank order, which is the
+//      left fold of the holders' values.  Then the members are placed into
 //      their partitions' runs: through per-lane partition counters where
 //      bins hold few entries, partition by partition from per-partition
 //      member bitmaps where they hold many, and by a counting sort above 32
@@ -608,7 +609,7 @@ __device__ __forceinline__ float averaged(float v, float fn, float inv) {
   return v;
 }
 
-constexpr int kWriteChunks = 8;
+constexpr int kWriteChunks = 12;  // chunk loads per batch (4, 8, 12, 16 measured on C5b; 12 fastest)
 // Average entries per 1024-key bin from which the writer emits partition by
 // partition (kPlaceMask): measured on the C4 embedding lists (82 entries a
 // bin, per-lane counters faster) and the C5b top-k lists (819 a bin, the
@@ -983,7 +984,7 @@ bin_write_kernel(const __grid_constant__ Lists lists, int n, int log_w, int bins
 // one-CTA reduction measured slower on C4: the extra launch costs more than
 // the atomics).
 constexpr int kDensWarps = 4;
-constexpr int kDensChunks = 8;
+constexpr int kDensChunks = 12;   // as the writer's
 
 // Bits 0, 2^L, 2 * 2^L, ... of a holder mask: the first rank of every group
 // of 2^L consecutive ranks.
@@ -1034,7 +1035,7 @@ densify_kernel(const __grid_constant__ Lists lists, int n, int log_w, int bins,
       }
     }
     __syncwarp();
-    // Rank by rank in chunks of up to 32 entries (walk_bin, 8 chunks' loads
+    // Rank by rank in chunks of up to 32 entries (walk_bin, 12 chunks' loads
     // in flight): a list is strictly ascending, so the lanes of one chunk
     // hold distinct keys and a plain read-modify-write of the mask is
     // race-free; chunks are ordered by a warp barrier.  A key whose mask was
