@@ -128,90 +128,96 @@ SparseLayout sparse_layout(int n, int64_t bins, int parts) {
 
 
 // ------------------------------------------------------------ 1. starts
-// Grid: x over groups of 4 positions (the last group holds position nnz,
-// the end marker), y = rank.  starts[r][b] = first position whose key is in
-// bin >= b (nnz if none); every list is checked strictly ascending and in
-// range.  32-bit index arithmetic throughout (positions, keys and bins all
-// fit).
+// Grid: x over groups of 4 positions, y = rank.  starts[r][b] = first
+// position whose key is in bin >= b (nnz if none); every list is checked
+// strictly ascending and in range.  32-bit index arithmetic throughout
+// (positions, keys and bins all fit).
+//
+// The groups of 4 real keys are grid-strided, kStartsUnroll per thread and
+// step (their loads issued together): per key a range and order check, its
+// bin (clamped, so out-of-range keys cannot address past the row) and, at a
+// bin change, the row entries of the bins it starts (more than one only
+// across empty bins).  CTA 0 then takes the ragged tail (the last nnz mod 4
+// keys) on one thread and the end marker, position nnz, which starts every
+// bin after the last key's, on all of its threads.
+__device__ __forceinline__ int clamped_bin(int key, int log_w, int bins) {
+  return min(max(key >> log_w, -1), bins);  // a negative key gives -1
+}
+
 __global__ void __launch_bounds__(256)
 bin_starts_kernel(const __grid_constant__ Lists lists, int dense_size, int log_w, int bins,
                   int32_t* starts, int32_t* status) {
+  __shared__ int s_last_bin;
   const int r = blockIdx.y;
   const int nnz = (int)lists.nnz[r];
   const int32_t* idx = lists.idx[r];
   int32_t* row = starts + (size_t)r * (bins + 1);
   const bool vec = (reinterpret_cast<uintptr_t>(idx) & 15) == 0;
-  const int groups = nnz / 4 + 1;
-  // Each thread takes kStartsUnroll groups per step (their loads issued
-  // together), so that one wave of CTAs keeps enough bytes in flight.  The
-  // boundary logic has no per-lane branches: a bin change stores one row
-  // entry (predicated), and the rare runs of empty bins are filled only
-  // when some lane of the warp has one.  The loop condition is the same
-  // for the whole warp, so every lane reaches the warp votes.
+  const int full = nnz >> 2;  // groups of 4 real keys
   constexpr int kU = kStartsUnroll;
   const int stride = gridDim.x * blockDim.x;
-  const int warp_q0 = (blockIdx.x * blockDim.x + threadIdx.x) & ~31;
-  for (int step = 0; warp_q0 + step * kU * stride < groups; ++step) {
-    const int q0 = blockIdx.x * blockDim.x + threadIdx.x + step * kU * stride;
+  bool bad = false;
+  for (int q0 = blockIdx.x * blockDim.x + threadIdx.x; q0 < full; q0 += kU * stride) {
     int4 kv[kU];
     int prev[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int q = q0 + u * stride;
-      const int i0 = q * 4;
       kv[u] = make_int4(0, 0, 0, 0);
       prev[u] = -1;
-      if (q < groups) {
-        if (vec && i0 + 4 <= nnz) {
+      if (q < full) {
+        if (vec) {
           kv[u] = __ldg(reinterpret_cast<const int4*>(idx) + q);
         } else {
-          if (i0 < nnz) kv[u].x = __ldg(idx + i0);
-          if (i0 + 1 < nnz) kv[u].y = __ldg(idx + i0 + 1);
-          if (i0 + 2 < nnz) kv[u].z = __ldg(idx + i0 + 2);
-          if (i0 + 3 < nnz) kv[u].w = __ldg(idx + i0 + 3);
+          kv[u].x = __ldg(idx + 4 * q);
+          kv[u].y = __ldg(idx + 4 * q + 1);
+          kv[u].z = __ldg(idx + 4 * q + 2);
+          kv[u].w = __ldg(idx + 4 * q + 3);
         }
-        if (i0 > 0) prev[u] = __ldg(idx + i0 - 1);
+        if (q > 0) prev[u] = __ldg(idx + 4 * q - 1);
       }
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int q = q0 + u * stride;
-      const int i0 = q * 4;
-      const bool in_range = q < groups;
+      if (q >= full) continue;
       const int key[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
-      // p: the key before position i (-1 before the first), bp its bin.
       int p = prev[u];
-      int bp = p < 0 ? -1 : min(p >> log_w, bins);
-      bool bad = false, gap = false;
-      int gap_lo[4], gap_hi[4];
+      int bp = p < 0 ? -1 : clamped_bin(p, log_w, bins);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int i = i0 + e;
-        const bool real = in_range && i < nnz;
-        // p >= key also rejects a negative first key (p is -1 there)
-        bad |= real && (key[e] >= dense_size || key[e] <= p);
-        // position nnz is the end marker: it starts every remaining bin;
-        // positions past it change nothing
-        int bk = bp;
-        if (real) bk = key[e] < 0 ? -1 : min(key[e] >> log_w, bins);
-        else if (in_range && i == nnz) bk = bins;
-        // a bin change at position i starts bins bp + 1 .. bk there; the
-        // first is stored here, the rest (empty bins) below
-        if (bk > bp) row[bp + 1] = i;
-        gap_lo[e] = bp + 2;
-        gap_hi[e] = bk;
-        gap |= bk > bp + 1;
-        bp = max(bp, bk);
-        if (real) p = key[e];
+        const int k = key[e];
+        // p >= k also rejects a negative first key (p is -1 there)
+        bad |= (unsigned)k >= (unsigned)dense_size || k <= p;
+        const int bk = clamped_bin(k, log_w, bins);
+        if (bk > bp) {
+          row[bp + 1] = 4 * q + e;
+          for (int bb = bp + 2; bb <= bk; ++bb) row[bb] = 4 * q + e;  // empty bins
+          bp = bk;
+        }
+        p = k;
       }
-      if (__any_sync(0xffffffffu, gap)) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          for (int bb = gap_lo[e]; bb <= gap_hi[e]; ++bb) row[bb] = i0 + e;
-      }
-      if (__any_sync(0xffffffffu, bad) && bad) flag(status, ZR_ERR_INPUT_UNSORTED);
     }
   }
+  if (blockIdx.x == 0) {
+    if (threadIdx.x == 0) {
+      int p = full > 0 ? __ldg(idx + 4 * full - 1) : -1;
+      int bp = p < 0 ? -1 : clamped_bin(p, log_w, bins);
+      for (int i = 4 * full; i < nnz; ++i) {
+        const int k = __ldg(idx + i);
+        bad |= (unsigned)k >= (unsigned)dense_size || k <= p;
+        const int bk = clamped_bin(k, log_w, bins);
+        for (int bb = bp + 1; bb <= bk; ++bb) row[bb] = i;
+        bp = max(bp, bk);
+        p = k;
+      }
+      s_last_bin = bp;
+    }
+    __syncthreads();
+    // the end marker: position nnz starts every bin after the last key's
+    for (int bb = s_last_bin + 1 + threadIdx.x; bb <= bins; bb += blockDim.x) row[bb] = nnz;
+  }
+  if (bad) flag(status, ZR_ERR_INPUT_UNSORTED);
 }
 
 // ------------------------------------------------------------ bin walk
