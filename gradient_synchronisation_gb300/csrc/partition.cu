@@ -282,13 +282,16 @@ struct PartShared {
 };
 constexpr size_t kPartSmem = sizeof(PartShared);
 
-// Loads tile [t0, t0 + len) of the list into shared memory and hashes it.
-__device__ void part_load(const PartArgs& A, PartShared& S, long long t0, int len) {
+// Loads tile [t0, t0 + len) of the list into shared memory and hashes it;
+// the values only when with_val (the count pass of a slice that does not
+// stay in shared memory across the wait needs the keys alone).
+__device__ void part_load(const PartArgs& A, PartShared& S, long long t0, int len,
+                          bool with_val) {
   for (int i = threadIdx.x; i < len; i += kT) {
     const long long pos = t0 + i;
     const int32_t k = A.idx ? __ldcs(A.idx + pos) : (int32_t)pos;
     S.key[i] = k;
-    if (A.val) S.val[i] = __ldcs(A.val + pos);
+    if (A.val && with_val) S.val[i] = __ldcs(A.val + pos);
     S.part[i] = (uint8_t)A.h((uint32_t)k);
   }
   __syncthreads();
@@ -312,7 +315,7 @@ __global__ void __launch_bounds__(kT, 1) partition_kernel(const __grid_constant_
   const int lane = tid & 31, warp = tid >> 5;
   for (long long t0 = lo; t0 < hi; t0 += kPTile) {
     const int tl = (int)min((long long)kPTile, hi - t0);
-    part_load(A, S, t0, tl);
+    part_load(A, S, t0, tl, resident);
     const int i0 = tid * kPPer, i1 = min(i0 + kPPer, tl);
     for (int s0 = 0; s0 < A.parts; s0 += kSlab) {
       counters_clear(S.cw);
@@ -343,7 +346,7 @@ __global__ void __launch_bounds__(kT, 1) partition_kernel(const __grid_constant_
   // place: per tile, thread t owns entries [kPPer t, kPPer (t + 1)) (input order)
   for (long long t0 = lo; t0 < hi; t0 += kPTile) {
     const int tl = (int)min((long long)kPTile, hi - t0);
-    if (!resident) part_load(A, S, t0, tl);
+    if (!resident) part_load(A, S, t0, tl, true);
     const int i0 = tid * kPPer, i1 = min(i0 + kPPer, tl);
     if (tid == 0) S.run = 0;
     for (int s0 = 0; s0 < A.parts; s0 += kSlab) {

@@ -1010,13 +1010,16 @@ __device__ __forceinline__ int popc_mask(uint32_t m) { return __popc(m); }
 __device__ __forceinline__ int popc_mask(unsigned long long m) { return __popcll(m); }
 
 // M: the holder mask type (32-bit up to 32 ranks, else 64-bit); kLogN:
-// log2 of the rank count.  Per warp: masks mk[W] and the list of the bin's
-// keys in first-holder order, mlist[W] (u16).
-template <typename M, int kLogN>
+// log2 of the rank count; kFlat: the flattened walk (lists with few entries
+// per bin on average) or the rank-by-rank walk.  Per warp: masks mk[W] and
+// the list of the bin's keys in first-holder order, mlist[W] (u16).
+template <typename M, int kLogN, bool kFlat>
 __global__ void __launch_bounds__(kDensWarps * 32)
 densify_kernel(const __grid_constant__ Lists lists, int n, int log_w, int bins,
-               const int32_t* starts, int64_t total_nnz, unsigned long long* counts) {
+               const int32_t* starts, int64_t total_nnz, unsigned long long* counts,
+               int32_t* status) {
   extern __shared__ __align__(16) unsigned char dens_smem[];
+  __shared__ BinRanks flat_all[kFlat ? kDensWarps : 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int W = 1 << log_w;
   M* mk = reinterpret_cast<M*>(dens_smem + (size_t)warp * W * (sizeof(M) + 2));
@@ -1041,6 +1044,37 @@ densify_kernel(const __grid_constant__ Lists lists, int n, int log_w, int bins,
       }
     }
     __syncwarp();
+    int members = 0;
+    BinFetch fetch;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      fetch.lo[h] = lo[h];
+      fetch.hi[h] = hi[h];
+    }
+    if (kFlat) {
+      BinRanks& F = flat_all[warp];
+      const int total = bin_commit(lists, n, fetch, F);
+      // Sparse bins: the flattened walk (groups of 32 entries across rank
+      // boundaries, as the writer's), the masks ORed with shared-memory
+      // atomics, since two lanes of a group may hold one key; the atomic's
+      // old value says which entry is the key's first holder.
+      int fkey[kBatch];
+      for_bin_entries(
+          lists, n, F, total, status,
+          [&](int t, int r, int pos) { fkey[t] = __ldg(lists.idx[r] + pos); },
+          [&](int, const int (&rank)[kBatch]) {
+#pragma unroll
+            for (int t = 0; t < kBatch; ++t) {
+              const uint32_t slot = (uint32_t)fkey[t] - base;
+              bool first = false;
+              if (rank[t] >= 0 && slot < (uint32_t)W)
+                first = atomicOr(&mk[slot], (M)1 << rank[t]) == 0;
+              const unsigned fresh = __ballot_sync(0xffffffffu, first);
+              if (first) mlist[members + __popc(fresh & lt)] = (uint16_t)slot;
+              members += __popc(fresh);
+            }
+          });
+    } else {
     // Rank by rank in chunks of up to 32 entries (walk_bin, 12 chunks' loads
     // in flight): a list is strictly ascending, so the lanes of one chunk
     // hold distinct keys and a plain read-modify-write of the mask is
@@ -1053,7 +1087,6 @@ densify_kernel(const __grid_constant__ Lists lists, int n, int log_w, int bins,
       R.len[h] = hi[h] - lo[h];
     }
     int key[kDensChunks], rk[kDensChunks];
-    int members = 0;
     walk_bin<kDensChunks>(
         R, n,
         [&](int t, int r, int pos) {
@@ -1072,6 +1105,7 @@ densify_kernel(const __grid_constant__ Lists lists, int n, int log_w, int bins,
           if (first) mlist[members + __popc(fresh & lt)] = (uint16_t)slot;
           members += __popc(fresh);
         });
+    }
     __syncwarp();
     // every member: fold its mask level by level and count the groups
     for (int j = lane; j < members; j += 32) {
@@ -1250,16 +1284,21 @@ zr_status sparse_launch(const int32_t* const* idx, const float* const* val, cons
 
 // The densification kernel for the rank count: 32-bit masks up to 32 ranks
 // (log2 n <= 5), 64-bit masks above (log2 n = 6).
-const void* densify_fn(bool wide, int logn) {
-  if (wide) return (const void*)densify_kernel<unsigned long long, 6>;
+template <bool kFlat>
+const void* densify_fn_walk(bool wide, int logn) {
+  if (wide) return (const void*)densify_kernel<unsigned long long, 6, kFlat>;
   switch (logn) {
-    case 0: return (const void*)densify_kernel<uint32_t, 0>;
-    case 1: return (const void*)densify_kernel<uint32_t, 1>;
-    case 2: return (const void*)densify_kernel<uint32_t, 2>;
-    case 3: return (const void*)densify_kernel<uint32_t, 3>;
-    case 4: return (const void*)densify_kernel<uint32_t, 4>;
-    default: return (const void*)densify_kernel<uint32_t, 5>;
+    case 0: return (const void*)densify_kernel<uint32_t, 0, kFlat>;
+    case 1: return (const void*)densify_kernel<uint32_t, 1, kFlat>;
+    case 2: return (const void*)densify_kernel<uint32_t, 2, kFlat>;
+    case 3: return (const void*)densify_kernel<uint32_t, 3, kFlat>;
+    case 4: return (const void*)densify_kernel<uint32_t, 4, kFlat>;
+    default: return (const void*)densify_kernel<uint32_t, 5, kFlat>;
   }
+}
+
+const void* densify_fn(bool wide, int logn, bool flat) {
+  return flat ? densify_fn_walk<true>(wide, logn) : densify_fn_walk<false>(wide, logn);
 }
 
 // Densification workspace: [status] then the bin starts (the sparse
@@ -1306,27 +1345,30 @@ zr_status densify_launch(const int32_t* const* idx, const int64_t* nnz, int n, i
   const bool wide = n > 32;
   const size_t per_key = (wide ? 8 : 4) + 2;  // mask + member list entry
   const size_t smem = (size_t)kDensWarps * ((size_t)1 << g.log_w) * per_key;
-  const void* fn = densify_fn(wide, logn);
+  // lists with few entries per bin on average take the flattened walk
+  const bool flat = total_nnz < kMaskMinPerBin * g.bins;
+  const void* fn = densify_fn(wide, logn, flat);
   static std::atomic<bool> attr_set[64];
   static std::mutex attr_lock;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ZR_ERR_CUDA;
   if (!attr_set[dev].load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> guard(attr_lock);
-    for (int lg = 0; lg <= 5; ++lg)
-      for (int wd = 0; wd < 2; ++wd)
-        if (cudaFuncSetAttribute(densify_fn(wd == 1, lg),
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)((size_t)kDensWarps * 4096 * (wd ? 10 : 6))) != cudaSuccess)
-          return ZR_ERR_CUDA;
+    for (int fl = 0; fl < 2; ++fl)
+      for (int lg = 0; lg <= 5; ++lg)
+        for (int wd = 0; wd < 2; ++wd)
+          if (cudaFuncSetAttribute(densify_fn(wd == 1, lg, fl == 1),
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)((size_t)kDensWarps * 4096 * (wd ? 10 : 6))) != cudaSuccess)
+            return ZR_ERR_CUDA;
     attr_set[dev].store(true, std::memory_order_release);
   }
   const int64_t units = (g.bins + kDensWarps - 1) / kDensWarps;
   const unsigned grid = (unsigned)grid_for(units, per_sm(fn, kDensWarps * 32, smem));
   int log_w = g.log_w;
   unsigned long long* counts = reinterpret_cast<unsigned long long*>(d_union_counts);
-  void* args[] = {(void*)&lists, (void*)&n, (void*)&log_w, (void*)&bins, (void*)&starts,
-                  (void*)&total_nnz, (void*)&counts};
+  void* args[] = {(void*)&lists, (void*)&n,         (void*)&log_w,  (void*)&bins,
+                  (void*)&starts, (void*)&total_nnz, (void*)&counts, (void*)&status};
   if (cudaLaunchKernel(fn, dim3(grid), dim3(kDensWarps * 32), args, smem, stream) != cudaSuccess)
     return ZR_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? ZR_OK : ZR_ERR_CUDA;
