@@ -90,6 +90,8 @@ constexpr int kChunkLog = 11;            // bins per scan chunk = 2048
 constexpr int kChunkBins = 1 << kChunkLog;
 constexpr int kScanThreads = kChunkBins / 2;
 
+constexpr int64_t kWidenBelowPerBin = 128;  // densification: entries per 1024-key bin below which bins widen
+
 struct Geometry {
   int log_w;
   int64_t bins;
@@ -97,12 +99,26 @@ struct Geometry {
 
 Geometry geometry(int n, int64_t dense_size, int parts, int64_t total_nnz) {
   Geometry g;
-  (void)total_nnz;
   g.log_w = 10;
   for (;;) {
     g.bins = (dense_size + (1ll << g.log_w) - 1) >> g.log_w;
     if (g.log_w >= 12 || g.bins * (int64_t)(parts + n) <= (1ll << 24)) break;
     ++g.log_w;
+  }
+  (void)total_nnz;
+  return g;
+}
+
+// Densification of lists with few entries per 1024-key bin (known at
+// launch) takes 2048-key bins: half the bins for the same entries (C4:
+// 0.038 -> 0.036 ms; the union's writer measured no faster, its occupancy
+// falls with the wider window).  The workspace is sized for the narrowest
+// bins, so it holds the wider ones.
+Geometry densify_geometry(int n, int64_t dense_size, int64_t total_nnz) {
+  Geometry g = geometry(n, dense_size, 0, total_nnz);
+  if (g.log_w == 10 && total_nnz >= 0 && total_nnz < kWidenBelowPerBin * g.bins) {
+    g.log_w = 11;
+    g.bins = (dense_size + (1ll << g.log_w) - 1) >> g.log_w;
   }
   return g;
 }
@@ -1324,7 +1340,7 @@ zr_status densify_launch(const int32_t* const* idx, const int64_t* nnz, int n, i
   }
   int logn = 0;
   while ((1 << logn) < n) ++logn;
-  const Geometry g = geometry(n, dense_size, 0, total_nnz);
+  const Geometry g = densify_geometry(n, dense_size, total_nnz);
   const SparseLayout L = sparse_layout(n, g.bins, 1);
   unsigned char* w = static_cast<unsigned char*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(w);
