@@ -39,7 +39,6 @@
 #include <stdint.h>
 
 #include <atomic>
-#include <mutex>
 
 #include "zr.h"
 #include "zr_device.cuh"
